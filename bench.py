@@ -1,0 +1,544 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE finalize (+ RMSNorm) path on GB300.
+
+Default workload: finalize + RMSNorm over 32768 tokens, hidden 4096, top-k 8,
+gemm2_permuted BF16 [288358, 4096] ~N(0, 2) (262144 indexed rows plus 10%
+never-indexed padding rows), a random permutation index map with 1% invalid
+slots, FP32 softmax weights, norm_weight ~N(0, 0.1), gain_center 1.0,
+eps 1e-6.  One step = one call over the whole batch; weight_before_norm
+alternates between steps so both orderings are timed.  The inputs (2.42 GB
+per call) are larger than L2, so every call reads its rows from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload roofline|padded|beam|small|decode] [--tokens T]
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle (the
+reference arm of this path) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth_inputs as si  # noqa: E402
+
+METRIC = "finalize tokens/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "moe_finalize_rmsnorm_gb300", "csrc")
+PROFILES = os.path.join(ROOT, "profiles")
+
+
+# ---------------------------------------------------------------------------
+# host-side helpers (also exercised by the CPU tests)
+
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Each rank finalizes its own independent batch (weak scaling)."""
+    return base_seed + 1000003 * rank
+
+
+def reduce_max(value: float, group=None) -> float:
+    """Max of a per-rank float over the default process group (identity at N=1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    dev = "cuda" if dist.get_backend(group) == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return float(t.item())
+
+
+def source_digest() -> str:
+    """Digest of the kernel sources; a recorded traffic figure applies only
+    to the sources it was measured on."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    recorded from an ncu capture in profiles/*.md, if it matches the current
+    sources.  Lines look like:
+    ``traffic: kernel=<name> workload=<name> bytes_per_launch=<n> sources=<digest>``"""
+    if not os.path.isdir(PROFILES):
+        return None
+    digest = source_digest()
+    pat = re.compile(r"traffic: kernel=(\S+) workload=(\S+) bytes_per_launch=(\d+) sources=(\S+)")
+    for name in sorted(os.listdir(PROFILES)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(PROFILES, name)) as f:
+            for line in f:
+                m = pat.search(line)
+                if m and m.group(1) == kernel and m.group(2) == workload and m.group(4) == digest:
+                    return float(m.group(3))
+    return None
+
+
+def measured_peaks() -> tuple[float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 50 ms in the background."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = (uuid or "").lower().replace("gpu-", "")
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+        self.error = None
+
+    def start(self) -> None:
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError as e:
+            self.error = f"nvidia-smi unavailable: {e}"
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.time()
+        while not self.samples and time.time() - t0 < 10 and self.proc.poll() is None:
+            time.sleep(0.02)
+
+    def _read(self) -> None:
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self) -> None:
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        if self.error:
+            return {"unavailable": self.error}
+        mine = [p for _, p in self.samples if not self.uuid or p[0].lower().replace("gpu-", "") == self.uuid]
+        if not mine:
+            mine = [p for _, p in self.samples]
+        inwin = [p for (t, p) in self.samples if t0 <= t <= t1 and p in mine]
+        use = inwin or mine
+        if not use:
+            return {"unavailable": "no nvidia-smi samples"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(p[1]) for p in use) if v is not None]
+        mx = [v for v in (num(p[2]) for p in use) if v is not None]
+        pw = [v for v in (num(p[3]) for p in use) if v is not None]
+        reasons = sorted({name for p in use for name, v in zip(self.REASONS, p[5:9])
+                          if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inwin)}
+
+
+def gpu_uuid(device_index: int) -> str | None:
+    import torch
+    try:
+        return str(torch.cuda.get_device_properties(device_index).uuid)
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# workloads
+
+class Job:
+    """Device-resident inputs of one workload and how to launch one step."""
+
+    def __init__(self, name, units_per_step, bytes_per_launch, kernel, launch, host, describe):
+        self.name = name
+        self.units_per_step = units_per_step
+        self.bytes_per_launch = bytes_per_launch
+        self.kernel = kernel
+        self.launch = launch
+        self.host = host
+        self.describe = describe
+
+
+def _dev_bf16(torch, bits, device):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(
+        device)
+
+
+def make_tp_job(torch, mf, case: si.TpCase, device, variant: str, alternate: bool) -> Job:
+    g = _dev_bf16(torch, case.gemm2, device)[:, :case.hidden]
+    w = (_dev_bf16(torch, case.weights, device) if case.weights.dtype == np.uint16
+         else torch.from_numpy(case.weights).to(device))
+    idx = torch.from_numpy(case.idx).to(device)
+    nw = _dev_bf16(torch, case.norm_weight, device)
+    out = torch.empty((case.num_tokens, case.hidden), dtype=torch.bfloat16, device=device)
+    T = case.num_tokens
+    wbytes = 2 if case.weights.dtype == np.uint16 else 4
+
+    def launch(step: int, tensors=(g, w, idx, nw, out)):
+        before = (step % 2 == 1) if alternate else case.weight_before_norm
+        gg, ww, ii, nn, oo = tensors
+        mf.moe_finalize_rmsnorm(gg, ww, ii, nn, oo, eps=case.eps, gain_center=case.gain_center,
+                                weight_before_norm=before, variant=variant)
+
+    chosen = mf.select_finalize_variant(T) if variant == "auto" else variant
+    kernel = {"bulk_ring": "tp_ring_kernel", "token_cta": "tp_token_cta_kernel",
+              "cluster": "tp_cluster_kernel"}[chosen]
+    job = Job(case.name, T, si.algorithmic_bytes_tp(T, case.hidden, case.top_k, wbytes), kernel,
+              launch, case, {"variant": chosen})
+    job.device_tensors = (g, w, idx, nw, out)
+    return job
+
+
+def make_beam_job(torch, mf, case: si.BeamCase, device, variant: str) -> Job:
+    cap, K, H = case.expert_outputs.shape
+    x = _dev_bf16(torch, case.expert_outputs, device)
+    w = torch.from_numpy(case.weights).to(device)
+    pw = _dev_bf16(torch, case.post_weight, device) if case.post_weight is not None else None
+    out = torch.empty((case.live_tokens, H), dtype=torch.bfloat16, device=device)
+
+    def launch(step: int, tensors=(x, w, pw, out)):
+        xx, ww, pp, oo = tensors
+        mf.beam_moe_finalize(xx, ww, oo, case.routed_scale, pp, case.post_eps, variant=variant)
+
+    chosen = mf.select_beam_variant(case.live_tokens, K, H) if variant == "auto" else variant
+    kernel = {"bulk_ring": "beam_ring_kernel", "token_cta": "beam_token_cta_kernel"}[chosen]
+    job = Job(case.name, case.live_tokens, si.algorithmic_bytes_beam(case.live_tokens, H, K),
+              kernel, launch, case, {"variant": chosen})
+    job.device_tensors = (x, w, pw, out)
+    return job
+
+
+def workload_case(name: str, tokens: int | None, seed_rank: int):
+    """Host inputs of a named workload (rank-dependent seed for N > 1)."""
+    if name == "roofline":
+        c = si.finalize_32768_tokens(False) if seed_rank == 0 else si.tp_case(
+            "finalize_T32768", si.ROOFLINE_TOKENS, indexed_rows=si.ROOFLINE_INDEXED_ROWS,
+            padding_rows=si.ROOFLINE_PADDING_ROWS, sigma=2.0, invalid_frac=0.01,
+            weights_dtype="fp32", gain_center=1.0, eps=1e-6, seed=seed_rank)
+        desc = ("finalize+RMSNorm num_tokens=32768 hidden=4096 top_k=8 gemm2=[288358,4096] "
+                "~N(0,2) 1% invalid fp32 weights gain_center=1.0 eps=1e-6, "
+                "weight_before_norm alternating per step")
+        return "tp", c, desc
+    if name == "padded":
+        return "tp", si.finalize_4096_tokens_padded(poison_padding=False), (
+            "finalize+RMSNorm num_tokens=4096 gemm2=[36864,4160] stride 4160, bf16 weights, "
+            "2% invalid, eps=1e-5, weight_before_norm=true")
+    if name == "small":
+        return "tp", si.finalize_16_tokens(), "finalize+RMSNorm num_tokens=16 gemm2=[128,4096]"
+    if name == "decode":
+        T = tokens or 1
+        return "tp", si.finalize_decode(T), f"finalize+RMSNorm decode num_tokens={T} rows={10 * T}"
+    if name == "beam":
+        return "beam", si.beam_8000_live(poison_dead_rows=False), (
+            "Beam finalize capacity=8192 top_k=8 hidden=7168 live_tokens=8000 routed_scale=2.5 "
+            "post-RMSNorm")
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline key)
+
+def time_oracle(kind: str, case, token_lo: int, token_hi: int, threads: int,
+                before: bool | None = None) -> float:
+    """Wall seconds for the oracle over tokens [lo, hi) split across threads."""
+    import oracle
+    n = token_hi - token_lo
+    chunks = max(1, min(threads, n))
+    bounds = [token_lo + (n * i) // chunks for i in range(chunks + 1)]
+
+    def work(i):
+        lo, hi = bounds[i], bounds[i + 1]
+        if hi <= lo:
+            return
+        if kind == "tp":
+            oracle.moe_finalize_rmsnorm(
+                case.gemm2, np.ascontiguousarray(case.weights[lo:hi]),
+                np.ascontiguousarray(case.idx[lo:hi]), case.norm_weight, eps=case.eps,
+                gain_center=case.gain_center,
+                weight_before_norm=case.weight_before_norm if before is None else before,
+                hidden=case.hidden)
+        else:
+            oracle.beam_moe_finalize(
+                np.ascontiguousarray(case.expert_outputs[lo:hi]),
+                np.ascontiguousarray(case.weights[lo:hi]), hi - lo,
+                routed_scale=case.routed_scale, post_weight=case.post_weight,
+                post_eps=case.post_eps)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(chunks) as ex:
+        list(ex.map(work, range(chunks)))
+    return time.perf_counter() - t0
+
+
+def total_tokens(kind, case):
+    return case.num_tokens if kind == "tp" else case.live_tokens
+
+
+def run_reference(args) -> None:
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    kind, case, desc = workload_case(args.workload, args.tokens, 0)
+    threads = os.cpu_count() or 1
+    T = total_tokens(kind, case)
+    # size each step so the whole run stays within about a minute of wall time
+    probe = min(T, max(threads, 64))
+    per_token = time_oracle(kind, case, 0, probe, threads) / probe
+    budget_s = 60.0
+    sample = int(max(1, min(T, budget_s / max(per_token, 1e-9) / max(args.steps + args.warmup, 1))))
+    lo = 0
+
+    def step(i):
+        nonlocal lo
+        if lo + sample > T:
+            lo = 0
+        before = (i % 2 == 1) if args.workload == "roofline" else None
+        s = time_oracle(kind, case, lo, lo + sample, threads, before)
+        lo += sample
+        return s
+
+    for i in range(args.warmup):
+        step(i)
+    secs = sum(step(i) for i in range(args.steps))
+    value = sample * args.steps / secs
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": desc, "tokens_per_step": sample},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{sample} consecutive tokens of the batch per step, "
+                                   f"{threads} threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+
+def run_ours(args) -> None:
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    from moe_finalize_rmsnorm_gb300.build import build
+    if rank == 0:
+        build()
+    if world > 1:
+        dist.barrier()
+    import moe_finalize_rmsnorm_gb300 as mf
+
+    kind, case, desc = workload_case(args.workload, args.tokens, rank_seed(0, rank) if rank else 0)
+    if kind == "tp":
+        job = make_tp_job(torch, mf, case, device, args.variant,
+                          alternate=args.workload == "roofline")
+    else:
+        job = make_beam_job(torch, mf, case, device, args.variant)
+    stream = torch.cuda.current_stream(device)
+
+    # warm-up
+    for i in range(args.warmup):
+        job.launch(i)
+    torch.cuda.synchronize(device)
+    if mf.device_status(clear=True) != 0:
+        raise SystemExit("device wait timeout during warm-up")
+
+    clocks = ClockSampler(gpu_uuid(local_rank))
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(device)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        job.launch(i)
+        ev[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    t_wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    clocks.stop()
+    if mf.device_status(clear=True) != 0:
+        raise SystemExit("device wait timeout in the timed region")
+
+    elapsed_ms = reduce_max(start.elapsed_time(end))
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    avg_launch_ms = statistics.fmean(launch_ms)
+    units = job.units_per_step * args.steps * world
+    value = units / (elapsed_ms / 1e3)
+    hbm_gbs = job.bytes_per_launch * args.steps / (elapsed_ms / 1e3) / 1e9
+    peak, peak_src = measured_peaks()
+    achieved = job.bytes_per_launch / (avg_launch_ms / 1e3) / 1e9
+    traffic = recorded_traffic(job.kernel, job.name)
+    extra = {}
+    if args.workload == "roofline":
+        extra["launch_us_by_ordering"] = {
+            "weight_before_norm=false": statistics.fmean(launch_ms[0::2]) * 1e3,
+            "weight_before_norm=true": statistics.fmean(launch_ms[1::2]) * 1e3
+            if len(launch_ms) > 1 else None}
+    extra["launch_us_p10_p50_p90"] = [float(np.percentile(launch_ms, q)) * 1e3 for q in (10, 50, 90)]
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": desc, "global_batch": job.units_per_step * world,
+                   "l2": "no flush: every step reads its inputs from HBM "
+                         f"({job.bytes_per_launch / 1e9:.3f} GB per launch, L2 is 0.13 GB)"
+                   if job.bytes_per_launch > 256e6 else "inputs smaller than L2 (warm)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   **job.describe},
+        "hbm_gbs": hbm_gbs,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic, "kernel": job.kernel,
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": job.bytes_per_launch},
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        **extra,
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(torch, mf, job, kind, case, device, args.e2e_steps)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        T = total_tokens(kind, case)
+        n = min(T, args.cpu_tokens)
+        secs = time_oracle(kind, case, 0, n, threads)
+        line["cpu_baseline"] = {"value": n / secs, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": f"the first {n} tokens of the same batch, one pass, "
+                                          f"{threads} threads ({secs:.2f} s wall)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_e2e(torch, mf, job: Job, kind: str, case, device, steps: int) -> dict:
+    """Same metric through the public API with host buffers: every step copies
+    its inputs from pinned host memory and reads the result back."""
+    dev = job.device_tensors
+    host = []
+    for t in dev:
+        host.append(None if t is None else torch.empty(t.shape, dtype=t.dtype).pin_memory())
+    # host copies of the inputs (the output's host buffer receives the result)
+    for h, d in zip(host[:-1], dev[:-1]):
+        if h is not None:
+            h.copy_(d.cpu() if d.is_contiguous() else d.contiguous().cpu())
+    ins = [(h, d) for h, d in zip(host[:-1], dev[:-1]) if h is not None]
+    out_h, out_d = host[-1], dev[-1]
+    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
+    d2h = out_h.numel() * out_h.element_size()
+    stream = torch.cuda.current_stream(device)
+
+    def step(i):
+        for h, d in ins:
+            d.copy_(h, non_blocking=True)
+        job.launch(i)
+        out_h.copy_(out_d, non_blocking=True)
+
+    step(0)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    ms = reduce_max(start.elapsed_time(end))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"value": job.units_per_step * steps * world / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": ms / steps}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default="roofline",
+                   choices=("roofline", "padded", "beam", "small", "decode"))
+    p.add_argument("--tokens", type=int, default=None, help="token count of --workload decode")
+    p.add_argument("--variant", default="auto", choices=("auto", "token_cta", "bulk_ring",
+                                                         "cluster"))
+    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-tokens", type=int, default=32768,
+                   help="tokens of the batch the CPU oracle baseline processes")
+    a = p.parse_args(argv)
+    a.warmup = max(3, a.warmup)  # at least three untimed warm-up steps
+    return a
+
+
+def main(argv=None) -> None:
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

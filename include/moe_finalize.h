@@ -1,0 +1,209 @@
+/*
+ * moe_finalize.h -- C ABI of the GB300 (sm_103a) MoE finalize library
+ * (libmoe_finalize.so).
+ *
+ * Two operations:
+ *
+ *   moe_finalize_rmsnorm  -- flashinfer.comm.tp_moe_finalize_rmsnorm (API
+ *     page: description and parameter list).  Per token t, gather the
+ *     unweighted GEMM2 rows selected by expanded_idx_to_permuted_idx[t, k],
+ *     scale each by its routing weight, reduce in FP32, apply RMSNorm with
+ *     gain norm_weight + gain_center (before or after the RMS), write BF16.
+ *
+ *   beam_moe_finalize     -- vllm.models.beam.nvidia.moe_finalize,
+ *     beam_moe_finalize (docstring and source).  Per live token, reduce a
+ *     token-major [capacity, top_k, hidden] block in FP32, round to BF16,
+ *     multiply by routed_scale and round to BF16 again, optionally apply a
+ *     post-RMSNorm, write BF16.
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are CUDA device (or managed) memory of the
+ *     current device; the caller owns all of them.  The library allocates no
+ *     memory and keeps no per-call state.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  No host synchronisation, no cross-stream ordering:
+ *     when switching streams, order the work with events, as the API page
+ *     requires of its own operation.
+ *   - Arguments are validated on the host before anything is launched.  On a
+ *     non-MF_OK return nothing was launched, except MF_ERR_CUDA, which reports
+ *     the launch error.
+ *   - A token count of zero is a no-op that returns MF_OK (pointers unchecked),
+ *     matching the Beam wrapper's "if output.shape[0]" guard.
+ *   - The output must not alias any input.
+ *   - Kernel waits are bounded (about two seconds of wall time); a wait that
+ *     gives up sets MF_ERR_DEVICE_TIMEOUT in the device status word, which
+ *     mf_device_status() reads.
+ *   - The first call on a device sets kernel attributes; make it before any
+ *     CUDA graph capture.  Captured calls replay with their arguments baked in.
+ */
+#ifndef MOE_FINALIZE_H
+#define MOE_FINALIZE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *mf_stream_t;
+
+typedef enum mf_status {
+    MF_OK = 0,
+    MF_ERR_NULL = 1,             /* a required pointer is NULL */
+    MF_ERR_SHAPE = 2,            /* sizes or strides break the tensor contract */
+    MF_ERR_ALIGN = 3,            /* a pointer breaks the 16-byte (or 4-byte) alignment rule */
+    MF_ERR_DTYPE = 4,            /* unknown weight dtype */
+    MF_ERR_UNSUPPORTED = 5,      /* hidden / top_k outside what the operation defines */
+    MF_ERR_CUDA = 6,             /* CUDA runtime error (no device, launch failure, ...) */
+    MF_ERR_DEVICE_TIMEOUT = 7,   /* a bounded device-side wait gave up */
+    MF_ERR_INVALID = 8           /* inconsistent argument combination or unknown variant */
+} mf_status;
+
+typedef enum mf_dtype {
+    MF_DTYPE_BF16 = 0,
+    MF_DTYPE_FP32 = 1
+} mf_dtype;
+
+/* Kernel choice.  AUTO picks by size; the others force one kernel (for
+ * validation and benchmarking, as the Beam wrappers' `strategy` argument
+ * forces a path).  A variant that does not apply returns MF_ERR_INVALID. */
+typedef enum mf_variant {
+    MF_VARIANT_AUTO = 0,
+    MF_VARIANT_TOKEN_CTA = 1,    /* one CTA per token, gathers held in registers */
+    MF_VARIANT_BULK_RING = 2,    /* persistent CTAs, bulk-copy ring of rows in shared memory */
+    MF_VARIANT_CLUSTER = 3       /* decode sizes: hidden split over a cluster, DSMEM reduction */
+} mf_variant;
+
+/*
+ * moe_finalize_rmsnorm -- flashinfer.comm.tp_moe_finalize_rmsnorm (API page,
+ * description and parameters gemm2_permuted, expert_weights,
+ * expanded_idx_to_permuted_idx, norm_weight, output, eps, gain_center,
+ * weight_before_norm), on one GPU (the page's tensor-parallel workspace does
+ * not apply to a single device: world size 1).
+ *
+ *   gemm2_permuted   device, BF16 [rows, row_stride] row-major: unweighted GEMM2
+ *                    rows in physical expert order.  Columns [0, hidden) are
+ *                    used; row_stride >= hidden, row_stride % 8 == 0, base
+ *                    16-byte aligned (so every row start is).  May be NULL
+ *                    only when rows == 0.
+ *   rows             number of rows; an index i is valid iff 0 <= i < rows.
+ *   expert_weights   device, [num_tokens, top_k] contiguous, BF16 or FP32
+ *                    (weights_dtype); converted to FP32.  16-byte aligned.
+ *   expanded_idx_to_permuted_idx
+ *                    device, int32 [num_tokens, top_k] contiguous, 16-byte
+ *                    aligned.  A negative or out-of-range index contributes
+ *                    zero and its weight is never read.
+ *   norm_weight      device, BF16 [hidden], 16-byte aligned.
+ *   output           device, BF16 [num_tokens, hidden] contiguous, 16-byte
+ *                    aligned.
+ *   hidden, top_k    must be 4096 and 8 (the operation is defined for these).
+ *   eps              added to the mean square inside the square root.
+ *   gain_center      added to norm_weight in FP32: g = float(norm_weight) + gain_center.
+ *   weight_before_norm  nonzero: y = v / rms(v) with v = acc * g;
+ *                    zero: y = acc / rms(acc) * g.
+ *
+ * For each token: acc[h] = sum over valid slots k, in ascending k, of
+ * w[t,k] * gemm2[idx[t,k], h] as FP32 fused multiply-adds; rms(v) =
+ * sqrt(mean_h v[h]^2 + eps) over the `hidden` columns; output = BF16(y)
+ * rounded to nearest even.
+ *
+ * Errors: MF_ERR_SHAPE (num_tokens < 0, rows < 0, row_stride < hidden or not
+ * a multiple of 8), MF_ERR_UNSUPPORTED (hidden != 4096 or top_k != 8),
+ * MF_ERR_NULL, MF_ERR_ALIGN, MF_ERR_DTYPE, MF_ERR_CUDA.
+ */
+mf_status moe_finalize_rmsnorm(const void *gemm2_permuted, int64_t rows, int64_t row_stride,
+                               const void *expert_weights, mf_dtype weights_dtype,
+                               const int32_t *expanded_idx_to_permuted_idx,
+                               const void *norm_weight, void *output, int64_t num_tokens,
+                               int32_t hidden, int32_t top_k, float eps, float gain_center,
+                               int weight_before_norm, mf_stream_t stream);
+
+/* moe_finalize_rmsnorm with an explicit kernel choice (same arguments and
+ * results; every variant gives the same output bits). */
+mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
+                                       int64_t row_stride, const void *expert_weights,
+                                       mf_dtype weights_dtype,
+                                       const int32_t *expanded_idx_to_permuted_idx,
+                                       const void *norm_weight, void *output,
+                                       int64_t num_tokens, int32_t hidden, int32_t top_k,
+                                       float eps, float gain_center, int weight_before_norm,
+                                       mf_variant variant, mf_stream_t stream);
+
+/*
+ * beam_moe_finalize -- vllm.models.beam.nvidia.moe_finalize, beam_moe_finalize
+ * (docstring: "reduce only output rows, preserving BF16 casts before scale
+ * and RMSNorm"; source: the argument assertions and the native call).
+ *
+ *   expert_outputs   device, BF16 [capacity, top_k, hidden] contiguous,
+ *                    token-major, 16-byte aligned.  Rows t >= live_tokens are
+ *                    never read.
+ *   capacity         first dimension of expert_outputs.
+ *   expert_weights   device, FP32 [weight_rows, top_k] contiguous, 4-byte
+ *                    aligned; weight_rows >= live_tokens.
+ *   output           device, BF16 [live_tokens, hidden] contiguous, 16-byte
+ *                    aligned.  Only these rows are written.
+ *   live_tokens      0 <= live_tokens <= capacity.
+ *   top_k            1 .. 32.
+ *   hidden           256 .. 8192, a multiple of 256.
+ *   routed_scale     multiplier applied to the BF16-rounded reduction.
+ *   post_weight      device BF16 [hidden] (16-byte aligned) or NULL; needs
+ *                    has_post_norm.
+ *   post_eps         RMSNorm epsilon (inside the square root).
+ *   has_post_norm    nonzero: apply the post-RMSNorm (unweighted when
+ *                    post_weight is NULL); zero: output = v.
+ *
+ * For each live token: s[h] = sum_k w[t,k] * x[t,k,h] (FP32 fused
+ * multiply-adds, ascending k); r = BF16(s); v = BF16(float(r) * routed_scale)
+ * (FP32 product); with the norm, output = BF16(v / sqrt(mean v^2 + post_eps)
+ * * post_weight), else output = v.
+ *
+ * Errors: MF_ERR_UNSUPPORTED (top_k or hidden out of range), MF_ERR_SHAPE
+ * (live_tokens < 0 or > capacity, weight_rows < live_tokens), MF_ERR_INVALID
+ * (post_weight without has_post_norm), MF_ERR_NULL, MF_ERR_ALIGN, MF_ERR_CUDA.
+ */
+mf_status beam_moe_finalize(const void *expert_outputs, int64_t capacity,
+                            const float *expert_weights, int64_t weight_rows, void *output,
+                            int64_t live_tokens, int32_t top_k, int32_t hidden,
+                            float routed_scale, const void *post_weight, float post_eps,
+                            int has_post_norm, mf_stream_t stream);
+
+/* beam_moe_finalize with an explicit kernel choice (TOKEN_CTA or BULK_RING). */
+mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity,
+                                    const float *expert_weights, int64_t weight_rows,
+                                    void *output, int64_t live_tokens, int32_t top_k,
+                                    int32_t hidden, float routed_scale, const void *post_weight,
+                                    float post_eps, int has_post_norm, mf_variant variant,
+                                    mf_stream_t stream);
+
+/* The kernel AUTO would run for moe_finalize_rmsnorm with num_tokens tokens
+ * on the current device (MF_VARIANT_AUTO if none would run). */
+mf_variant mf_select_finalize_variant(int64_t num_tokens);
+
+/* The kernel AUTO would run for beam_moe_finalize. */
+mf_variant mf_select_beam_variant(int64_t live_tokens, int32_t top_k, int32_t hidden);
+
+/* Human-readable name of a status code (static string). */
+const char *mf_status_string(mf_status status);
+
+/* Read the device status word of the current device after synchronising it:
+ * MF_OK, or MF_ERR_DEVICE_TIMEOUT if any kernel's bounded wait gave up since
+ * the word was last cleared.  Nonzero `clear` resets the word.  MF_ERR_CUDA
+ * if the device cannot be reached. */
+mf_status mf_device_status(int clear);
+
+/* Failure-detection self-test: launch one block whose thread waits on an
+ * mbarrier that nothing will ever complete, bounded by timeout_ns (clamped to
+ * at most one second).  The wait gives up, records MF_ERR_DEVICE_TIMEOUT in
+ * the device status word and the kernel returns normally; the context stays
+ * usable.  Read the result with mf_device_status(). */
+mf_status mf_selftest_wait_timeout(uint64_t timeout_ns, mf_stream_t stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t mf_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FINALIZE_H */

@@ -1,0 +1,155 @@
+"""GB300 (sm_103a) MoE finalize + RMSNorm and Beam finalize.
+
+Thin Python binding over the C ABI of ``libmoe_finalize.so``
+(include/moe_finalize.h): it checks tensor metadata, reads pointers, sizes
+and the current CUDA stream, and calls the library.  Every arithmetic step
+runs in the library's CUDA kernels; PyTorch only supplies device memory and
+streams.  There is no CPU fallback: without the built library the calls raise.
+
+* ``moe_finalize_rmsnorm`` (alias ``tp_moe_finalize_rmsnorm``) follows
+  flashinfer.comm.tp_moe_finalize_rmsnorm (API page), on one GPU.
+* ``beam_moe_finalize`` follows vllm.models.beam.nvidia.moe_finalize,
+  beam_moe_finalize.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._abi import (MF_DTYPE_BF16, MF_DTYPE_FP32, VARIANT_NAMES, VARIANTS, MoeFinalizeError,
+                   check, lib)
+
+__all__ = [
+    "moe_finalize_rmsnorm", "tp_moe_finalize_rmsnorm", "beam_moe_finalize", "MoeFinalizeError",
+    "device_status", "selftest_wait_timeout", "select_finalize_variant", "select_beam_variant",
+    "version", "HIDDEN", "TOP_K",
+]
+
+HIDDEN = 4096
+TOP_K = 8
+
+
+def _stream_ptr(stream, device) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _req(cond: bool, msg: str) -> None:
+    if not cond:
+        raise ValueError(msg)
+
+
+def _variant(name: str) -> int:
+    _req(name in VARIANTS, f"unknown variant {name!r}; one of {sorted(VARIANTS)}")
+    return VARIANTS[name]
+
+
+def moe_finalize_rmsnorm(gemm2_permuted: torch.Tensor, expert_weights: torch.Tensor,
+                         expanded_idx_to_permuted_idx: torch.Tensor, norm_weight: torch.Tensor,
+                         output: torch.Tensor, *, eps: float, gain_center: float,
+                         weight_before_norm: bool, variant: str = "auto",
+                         stream: torch.cuda.Stream | None = None) -> None:
+    """Finalize + RMSNorm into ``output`` (BF16 [num_tokens, 4096]).
+
+    gemm2_permuted: BF16 (rows, >= 4096), unit last-dim stride, row stride a
+    multiple of 8.  expert_weights: BF16 or FP32 (num_tokens, 8).
+    expanded_idx_to_permuted_idx: int32 (num_tokens, 8); negative or
+    out-of-range entries contribute zero.  norm_weight: BF16 (4096,).
+    Asynchronous on ``stream`` (default: the current stream).
+    """
+    g, w, idx, nw, out = gemm2_permuted, expert_weights, expanded_idx_to_permuted_idx, \
+        norm_weight, output
+    _req(g.dim() == 2 and g.dtype == torch.bfloat16 and (g.stride(1) == 1 or g.shape[1] <= 1),
+         "gemm2_permuted must be a 2-D BF16 tensor with unit last-dim stride")
+    _req(out.dim() == 2 and out.dtype == torch.bfloat16 and out.is_contiguous(),
+         "output must be a contiguous 2-D BF16 tensor")
+    _req(idx.dim() == 2 and idx.dtype == torch.int32 and idx.is_contiguous(),
+         "expanded_idx_to_permuted_idx must be a contiguous 2-D int32 tensor")
+    _req(w.dtype in (torch.bfloat16, torch.float32) and w.is_contiguous() and w.shape == idx.shape,
+         "expert_weights must be contiguous BF16 or FP32 with the index map's shape")
+    _req(nw.dim() == 1 and nw.dtype == torch.bfloat16 and nw.is_contiguous(),
+         "norm_weight must be a contiguous 1-D BF16 tensor")
+    _req(out.shape[0] == idx.shape[0], "output and the index map disagree on num_tokens")
+    _req(nw.shape[0] == out.shape[1], "norm_weight and output disagree on hidden")
+    dev = out.device
+    _req(dev.type == "cuda" and all(t.device == dev for t in (g, w, idx, nw)),
+         "all tensors must be on the same CUDA device")
+    row_stride = g.stride(0) if g.shape[0] > 1 else max(g.shape[1], g.stride(0))
+    with torch.cuda.device(dev):
+        st = lib().moe_finalize_rmsnorm_variant(
+            g.data_ptr(), g.shape[0], row_stride, w.data_ptr(),
+            MF_DTYPE_BF16 if w.dtype == torch.bfloat16 else MF_DTYPE_FP32, idx.data_ptr(),
+            nw.data_ptr(), out.data_ptr(), out.shape[0], out.shape[1], idx.shape[1], float(eps),
+            float(gain_center), int(bool(weight_before_norm)), _variant(variant),
+            _stream_ptr(stream, dev))
+    check(st, "moe_finalize_rmsnorm")
+
+
+tp_moe_finalize_rmsnorm = moe_finalize_rmsnorm
+
+
+def beam_moe_finalize(expert_outputs: torch.Tensor, expert_weights: torch.Tensor,
+                      output: torch.Tensor, routed_scale: float = 1.0,
+                      post_weight: torch.Tensor | None = None, post_eps: float | None = None, *,
+                      variant: str = "auto",
+                      stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Beam finalize of the live rows (``output.shape[0]``) into ``output``.
+
+    expert_outputs: contiguous BF16 [capacity, top_k, hidden].  expert_weights:
+    contiguous FP32 [>= live, top_k].  output: contiguous BF16 [live, hidden].
+    post_eps None omits the normalisation; post_weight None with post_eps set
+    is an unweighted RMSNorm.  Returns ``output``.
+    """
+    x, w, out = expert_outputs, expert_weights, output
+    _req(x.dim() == 3 and w.dim() == 2 and out.dim() == 2, "expected 3-D, 2-D, 2-D tensors")
+    _req(x.dtype == torch.bfloat16 and out.dtype == torch.bfloat16 and w.dtype == torch.float32,
+         "expert_outputs/output must be BF16 and expert_weights FP32")
+    _req(x.is_contiguous() and w.is_contiguous() and out.is_contiguous(),
+         "expert_outputs, expert_weights and output must be contiguous")
+    cap, top_k, hidden = x.shape
+    _req(out.shape[1] == hidden and w.shape[1] == top_k, "shapes disagree on hidden or top_k")
+    dev = out.device
+    _req(dev.type == "cuda" and x.device == dev and w.device == dev,
+         "all tensors must be on the same CUDA device")
+    pw_ptr = None
+    if post_weight is not None:
+        _req(post_eps is not None, "post_weight requires post_eps")
+        _req(post_weight.shape == (hidden,) and post_weight.is_contiguous() and
+             post_weight.dtype == torch.bfloat16 and post_weight.device == dev,
+             "post_weight must be a contiguous BF16 [hidden] tensor on the output's device")
+        pw_ptr = post_weight.data_ptr()
+    with torch.cuda.device(dev):
+        st = lib().beam_moe_finalize_variant(
+            x.data_ptr(), cap, w.data_ptr(), w.shape[0], out.data_ptr(), out.shape[0], top_k,
+            hidden, float(routed_scale), pw_ptr, float(post_eps or 0.0),
+            int(post_eps is not None), _variant(variant), _stream_ptr(stream, dev))
+    check(st, "beam_moe_finalize")
+    return out
+
+
+def select_finalize_variant(num_tokens: int) -> str:
+    """Kernel the automatic choice runs for ``num_tokens`` (current device)."""
+    return VARIANT_NAMES[lib().mf_select_finalize_variant(int(num_tokens))]
+
+
+def select_beam_variant(live_tokens: int, top_k: int, hidden: int) -> str:
+    return VARIANT_NAMES[lib().mf_select_beam_variant(int(live_tokens), int(top_k), int(hidden))]
+
+
+def device_status(clear: bool = True) -> int:
+    """Synchronise the current device and return its status word as a status
+    code (0, or 7 = MF_ERR_DEVICE_TIMEOUT if a bounded wait gave up)."""
+    return int(lib().mf_device_status(int(bool(clear))))
+
+
+def selftest_wait_timeout(timeout_ns: int = 10_000_000,
+                          stream: torch.cuda.Stream | None = None) -> None:
+    """Launch the failure-detection self-test (a wait that must give up)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    check(lib().mf_selftest_wait_timeout(int(timeout_ns), _stream_ptr(stream, dev)),
+          "mf_selftest_wait_timeout")
+
+
+def version() -> int:
+    return int(lib().mf_version())

@@ -1,0 +1,252 @@
+// C ABI of libmoe_finalize.so: argument validation, kernel selection and the
+// device status word.  Declarations and the contract are in
+// include/moe_finalize.h.
+
+#include <mutex>
+
+#include "../../include/moe_finalize.h"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace {
+
+// Device status word: kernels OR mf::kStatusWaitTimeout into it when a
+// bounded wait gives up.  One per device (module globals are per context).
+__device__ unsigned int g_status_word;
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s bound on every device wait
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int smem_optin = 0;
+    unsigned *status = nullptr;  // device address of g_status_word
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+
+// Per-device set-up on first use: SM count, opt-in shared memory, the status
+// word's device address and the kernels' attributes.
+mf_status device_info(const DeviceInfo **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MF_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess ||
+            cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status_word) !=
+                cudaSuccess ||
+            mf::prepare_tp_kernels(d.smem_optin) != cudaSuccess ||
+            mf::prepare_beam_kernels(d.smem_optin) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return MF_ERR_CUDA;
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return MF_OK;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Token counts at or below this use the cluster decode kernel; above it and
+// below kRingMinTokens the one-CTA-per-token kernel.
+constexpr int64_t kClusterMaxTokens = 64;
+constexpr int64_t kRingMinTokens = 1024;
+
+mf_variant pick_tp(int64_t num_tokens) {
+    if (num_tokens <= 0) return MF_VARIANT_AUTO;
+    if (num_tokens <= kClusterMaxTokens) return MF_VARIANT_CLUSTER;
+    if (num_tokens < kRingMinTokens) return MF_VARIANT_TOKEN_CTA;
+    return MF_VARIANT_BULK_RING;
+}
+
+mf_variant pick_beam(int64_t live, int num_sms) {
+    if (live <= 0) return MF_VARIANT_AUTO;
+    return live >= num_sms ? MF_VARIANT_BULK_RING : MF_VARIANT_TOKEN_CTA;
+}
+
+mf_status from_launch(cudaError_t e) { return e == cudaSuccess ? MF_OK : MF_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *mf_status_string(mf_status s) {
+    switch (s) {
+        case MF_OK: return "ok";
+        case MF_ERR_NULL: return "a required pointer is NULL";
+        case MF_ERR_SHAPE: return "sizes or strides break the tensor contract";
+        case MF_ERR_ALIGN: return "a pointer is not aligned as required";
+        case MF_ERR_DTYPE: return "unknown weight dtype";
+        case MF_ERR_UNSUPPORTED: return "hidden or top_k outside what the operation defines";
+        case MF_ERR_CUDA: return "CUDA runtime error";
+        case MF_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait timed out";
+        case MF_ERR_INVALID: return "inconsistent arguments or unknown variant";
+    }
+    return "unknown status";
+}
+
+int32_t mf_version(void) { return 100; }
+
+mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
+                                       int64_t row_stride, const void *expert_weights,
+                                       mf_dtype weights_dtype,
+                                       const int32_t *expanded_idx_to_permuted_idx,
+                                       const void *norm_weight, void *output,
+                                       int64_t num_tokens, int32_t hidden, int32_t top_k,
+                                       float eps, float gain_center, int weight_before_norm,
+                                       mf_variant variant, mf_stream_t stream) {
+    if (num_tokens < 0 || rows < 0) return MF_ERR_SHAPE;
+    if (hidden != mf::kTpHidden || top_k != mf::kTpTopK) return MF_ERR_UNSUPPORTED;
+    if (row_stride < hidden || row_stride % 8 != 0) return MF_ERR_SHAPE;
+    if (weights_dtype != MF_DTYPE_BF16 && weights_dtype != MF_DTYPE_FP32) return MF_ERR_DTYPE;
+    if (variant < MF_VARIANT_AUTO || variant > MF_VARIANT_CLUSTER) return MF_ERR_INVALID;
+    if (num_tokens == 0) return MF_OK;
+    if (!expert_weights || !expanded_idx_to_permuted_idx || !norm_weight || !output ||
+        (rows > 0 && !gemm2_permuted))
+        return MF_ERR_NULL;
+    if (!aligned(gemm2_permuted, 16) || !aligned(expert_weights, 16) ||
+        !aligned(expanded_idx_to_permuted_idx, 16) || !aligned(norm_weight, 16) ||
+        !aligned(output, 16))
+        return MF_ERR_ALIGN;
+    if (num_tokens > 0x7fffffffLL / 16) return MF_ERR_SHAPE;  // grid limits of the decode kernel
+
+    const DeviceInfo *d = nullptr;
+    mf_status st = device_info(&d);
+    if (st != MF_OK) return st;
+
+    mf::TpArgs a;
+    a.gemm2 = static_cast<const uint16_t *>(gemm2_permuted);
+    a.rows = rows;
+    a.ld = row_stride;
+    a.weights = expert_weights;
+    a.idx = expanded_idx_to_permuted_idx;
+    a.norm_weight = static_cast<const uint16_t *>(norm_weight);
+    a.out = static_cast<uint16_t *>(output);
+    a.num_tokens = num_tokens;
+    a.eps = eps;
+    a.gain_center = gain_center;
+    a.before = weight_before_norm ? 1 : 0;
+    a.status = d->status;
+    a.timeout_ns = kWaitLimitNs;
+    const bool bf16w = weights_dtype == MF_DTYPE_BF16;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    if (variant == MF_VARIANT_AUTO) variant = pick_tp(num_tokens);
+    switch (variant) {
+        case MF_VARIANT_CLUSTER: return from_launch(mf::launch_tp_cluster(a, bf16w, s));
+        case MF_VARIANT_TOKEN_CTA: return from_launch(mf::launch_tp_token_cta(a, bf16w, s));
+        case MF_VARIANT_BULK_RING:
+            return from_launch(mf::launch_tp_ring(a, bf16w, d->num_sms, d->smem_optin, s));
+        default: return MF_ERR_INVALID;
+    }
+}
+
+mf_status moe_finalize_rmsnorm(const void *gemm2_permuted, int64_t rows, int64_t row_stride,
+                               const void *expert_weights, mf_dtype weights_dtype,
+                               const int32_t *expanded_idx_to_permuted_idx,
+                               const void *norm_weight, void *output, int64_t num_tokens,
+                               int32_t hidden, int32_t top_k, float eps, float gain_center,
+                               int weight_before_norm, mf_stream_t stream) {
+    return moe_finalize_rmsnorm_variant(gemm2_permuted, rows, row_stride, expert_weights,
+                                        weights_dtype, expanded_idx_to_permuted_idx, norm_weight,
+                                        output, num_tokens, hidden, top_k, eps, gain_center,
+                                        weight_before_norm, MF_VARIANT_AUTO, stream);
+}
+
+mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity,
+                                    const float *expert_weights, int64_t weight_rows,
+                                    void *output, int64_t live_tokens, int32_t top_k,
+                                    int32_t hidden, float routed_scale, const void *post_weight,
+                                    float post_eps, int has_post_norm, mf_variant variant,
+                                    mf_stream_t stream) {
+    if (top_k < 1 || top_k > 32) return MF_ERR_UNSUPPORTED;
+    if (hidden < 256 || hidden > 8192 || hidden % 256 != 0) return MF_ERR_UNSUPPORTED;
+    if (capacity < 0 || live_tokens < 0 || live_tokens > capacity || weight_rows < live_tokens)
+        return MF_ERR_SHAPE;
+    if (post_weight && !has_post_norm) return MF_ERR_INVALID;
+    if (variant != MF_VARIANT_AUTO && variant != MF_VARIANT_TOKEN_CTA &&
+        variant != MF_VARIANT_BULK_RING)
+        return MF_ERR_INVALID;
+    if (live_tokens == 0) return MF_OK;
+    if (!expert_outputs || !expert_weights || !output) return MF_ERR_NULL;
+    if (!aligned(expert_outputs, 16) || !aligned(output, 16) || !aligned(expert_weights, 4) ||
+        (post_weight && !aligned(post_weight, 16)))
+        return MF_ERR_ALIGN;
+    if (live_tokens > 0x7fffffffLL) return MF_ERR_SHAPE;
+
+    const DeviceInfo *d = nullptr;
+    mf_status st = device_info(&d);
+    if (st != MF_OK) return st;
+
+    mf::BeamArgs a;
+    a.x = static_cast<const uint16_t *>(expert_outputs);
+    a.weights = expert_weights;
+    a.out = static_cast<uint16_t *>(output);
+    a.post_weight = static_cast<const uint16_t *>(post_weight);
+    a.live = live_tokens;
+    a.top_k = top_k;
+    a.hidden = hidden;
+    a.routed_scale = routed_scale;
+    a.post_eps = post_eps;
+    a.has_norm = has_post_norm ? 1 : 0;
+    a.status = d->status;
+    a.timeout_ns = kWaitLimitNs;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    if (variant == MF_VARIANT_AUTO) variant = pick_beam(live_tokens, d->num_sms);
+    if (variant == MF_VARIANT_BULK_RING)
+        return from_launch(mf::launch_beam_ring(a, d->num_sms, d->smem_optin, s));
+    return from_launch(mf::launch_beam_token_cta(a, s));
+}
+
+mf_status beam_moe_finalize(const void *expert_outputs, int64_t capacity,
+                            const float *expert_weights, int64_t weight_rows, void *output,
+                            int64_t live_tokens, int32_t top_k, int32_t hidden,
+                            float routed_scale, const void *post_weight, float post_eps,
+                            int has_post_norm, mf_stream_t stream) {
+    return beam_moe_finalize_variant(expert_outputs, capacity, expert_weights, weight_rows, output,
+                                     live_tokens, top_k, hidden, routed_scale, post_weight,
+                                     post_eps, has_post_norm, MF_VARIANT_AUTO, stream);
+}
+
+mf_variant mf_select_finalize_variant(int64_t num_tokens) { return pick_tp(num_tokens); }
+
+mf_variant mf_select_beam_variant(int64_t live_tokens, int32_t top_k, int32_t hidden) {
+    (void)top_k;
+    (void)hidden;
+    const DeviceInfo *d = nullptr;
+    if (device_info(&d) != MF_OK) return MF_VARIANT_AUTO;
+    return pick_beam(live_tokens, d->num_sms);
+}
+
+mf_status mf_device_status(int clear) {
+    const DeviceInfo *d = nullptr;
+    mf_status st = device_info(&d);
+    if (st != MF_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MF_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof word) != cudaSuccess) return MF_ERR_CUDA;
+    if (clear) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess)
+            return MF_ERR_CUDA;
+    }
+    return (word & mf::kStatusWaitTimeout) ? MF_ERR_DEVICE_TIMEOUT : MF_OK;
+}
+
+mf_status mf_selftest_wait_timeout(uint64_t timeout_ns, mf_stream_t stream) {
+    const DeviceInfo *d = nullptr;
+    mf_status st = device_info(&d);
+    if (st != MF_OK) return st;
+    if (timeout_ns > 1000000000ull) timeout_ns = 1000000000ull;
+    return from_launch(mf::launch_wait_timeout_selftest(d->status, timeout_ns,
+                                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+"""Host-side logic of bench.py (CPU only): the multi-rank timing reduction
+over a 2-rank gloo group, seeds per rank, the clock-sample summary and the
+recorded-traffic lookup."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, results):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        mx = bench.reduce_max(10.0 + rank)
+        results[rank] = (mx, bench.rank_seed(0, rank))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_reduce_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        results = m.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_rank_main, args=(r, 2, port, results)) for r in range(2)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        res = dict(results)
+    assert res[0][0] == res[1][0] == 11.0          # both ranks see the max
+    assert res[0][1] != res[1][1]                  # independent batches per rank
+
+
+def test_reduce_max_without_a_group_is_identity():
+    assert bench.reduce_max(3.5) == 3.5
+
+
+def test_clock_summary_prefers_the_timed_window():
+    c = bench.ClockSampler("GPU-abc")
+    row = ["GPU-abc", "1965", "2070", "900.5", "0x0", "Not Active", "Not Active", "Not Active",
+           "Active"]
+    idle = ["GPU-abc", "600", "2070", "100.0", "0x0", "Not Active", "Not Active", "Not Active",
+            "Not Active"]
+    other = ["GPU-zzz", "100", "2070", "50", "0x0", "Active", "Active", "Active", "Active"]
+    c.samples = [(1.0, idle), (2.0, row), (2.5, row), (2.6, other), (4.0, idle)]
+    s = c.summary(1.5, 3.0)
+    assert s["sm_mhz"] == 1965 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"] and s["samples_in_timed_region"] == 2
+
+
+def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
+    d = bench.source_digest()
+    (tmp_path / "k.md").write_text(
+        f"traffic: kernel=tp_ring_kernel workload=w bytes_per_launch=123 sources={d}\n"
+        "traffic: kernel=tp_ring_kernel workload=v bytes_per_launch=9 sources=stale\n")
+    assert bench.recorded_traffic("tp_ring_kernel", "w") == 123
+    assert bench.recorded_traffic("tp_ring_kernel", "v") is None
+    assert bench.recorded_traffic("other", "w") is None
+
+
+def test_parse_args_defaults_and_warmup_floor():
+    a = bench.parse_args([])
+    assert a.gpus == 1 and a.workload == "roofline" and a.impl == "ours" and a.warmup >= 3
+    assert bench.parse_args(["--warmup", "1"]).warmup == 3
+
+
+def test_algorithmic_bytes_formula():
+    import synth_inputs as si
+    # K*H*2 + H*2 + K*4 + K*4 per token with FP32 weights
+    assert si.algorithmic_bytes_tp(1) == 8 * 4096 * 2 + 4096 * 2 + 32 + 32 == 73792
+    assert si.algorithmic_bytes_tp(32768) == 2418016256
+    assert si.algorithmic_bytes_beam(8000, 7168, 8) == 8000 * 129056

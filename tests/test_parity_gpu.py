@@ -1,0 +1,348 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Every case runs the same seeded inputs through both and compares every
+output element: |gpu - oracle| <= 2^-7 |oracle| + 1e-6 and at least 99% of
+the elements bit-exact (the Beam path without normalisation must match bit
+for bit).  Outputs carry canary rows past their end that must stay untouched.
+"""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import synth_inputs as si
+from helpers import bf16_bits_to_f64, compare_bf16
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+CANARY = 0x1234
+TP_VARIANTS = ("cluster", "token_cta", "bulk_ring", "auto")
+BEAM_VARIANTS = ("token_cta", "bulk_ring", "auto")
+
+
+@pytest.fixture(scope="session", autouse=True)
+def cuda_lib():
+    if not torch.cuda.is_available():
+        pytest.fail("no CUDA device: the gpu tests need a GB300")
+    from moe_finalize_rmsnorm_gb300.build import build
+    build()
+    import moe_finalize_rmsnorm_gb300 as mf
+    assert mf.device_status(clear=True) == 0
+    yield mf
+    assert mf.device_status(clear=True) == 0, "a kernel's bounded wait timed out"
+
+
+def dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def host_bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def run_tp(mf, case, variant, *, before=None, stream=None):
+    before = case.weight_before_norm if before is None else before
+    T, H = case.num_tokens, case.hidden
+    g = dev_bf16(case.gemm2)[:, :H] if case.gemm2.size else \
+        torch.empty((0, H), dtype=torch.bfloat16, device="cuda")
+    w = dev_bf16(case.weights) if case.weights.dtype == np.uint16 else \
+        torch.from_numpy(case.weights).cuda()
+    idx = torch.from_numpy(case.idx).cuda()
+    nw = dev_bf16(case.norm_weight)
+    buf = torch.full((T + 2, H), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    out = buf[:T]
+    mf.moe_finalize_rmsnorm(g, w, idx, nw, out, eps=case.eps, gain_center=case.gain_center,
+                            weight_before_norm=before, variant=variant, stream=stream)
+    torch.cuda.synchronize()
+    got = host_bits(buf)
+    assert np.all(got[T:] == CANARY), "output canary overwritten"
+    return got[:T]
+
+
+def oracle_tp(case, before=None):
+    before = case.weight_before_norm if before is None else before
+    return oracle.moe_finalize_rmsnorm(case.gemm2, case.weights, case.idx, case.norm_weight,
+                                       eps=case.eps, gain_center=case.gain_center,
+                                       weight_before_norm=before, hidden=case.hidden)
+
+
+def run_beam(mf, case, variant, live=None):
+    live = case.live_tokens if live is None else live
+    cap, K, H = case.expert_outputs.shape
+    x = dev_bf16(case.expert_outputs)
+    w = torch.from_numpy(case.weights).cuda()
+    pw = dev_bf16(case.post_weight) if case.post_weight is not None else None
+    buf = torch.full((live + 2, H), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    out = buf[:live]
+    r = mf.beam_moe_finalize(x, w, out, case.routed_scale, pw, case.post_eps, variant=variant)
+    assert r.data_ptr() == out.data_ptr()
+    torch.cuda.synchronize()
+    got = host_bits(buf)
+    assert np.all(got[live:] == CANARY), "output canary overwritten"
+    return got[:live]
+
+
+def oracle_beam(case, live=None):
+    live = case.live_tokens if live is None else live
+    return oracle.beam_moe_finalize(case.expert_outputs, case.weights, live,
+                                    routed_scale=case.routed_scale, post_weight=case.post_weight,
+                                    post_eps=case.post_eps)
+
+
+# ---------------------------------------------------------------------------
+# the five workloads
+
+@functools.lru_cache(maxsize=None)
+def c_small():
+    return si.finalize_16_tokens()
+
+
+@functools.lru_cache(maxsize=1)
+def c_padded():
+    return si.finalize_4096_tokens_padded(poison_padding=True)
+
+
+@functools.lru_cache(maxsize=None)
+def c_decode(T):
+    return si.finalize_decode(T)
+
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_finalize_16_tokens(cuda_lib, variant):
+    case = c_small()
+    compare_bf16(run_tp(cuda_lib, case, variant), oracle_tp(case))
+
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_finalize_4096_tokens_padded_stride_bf16_weights(cuda_lib, variant):
+    case = c_padded()
+    got = run_tp(cuda_lib, case, variant)
+    assert not np.isnan(bf16_bits_to_f64(got)).any(), "padding (NaN) leaked into the output"
+    compare_bf16(got, oracle_tp(case))
+
+
+@pytest.mark.parametrize("T", si.DECODE_TOKENS)
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_finalize_decode_sizes(cuda_lib, T, variant):
+    case = c_decode(T)
+    compare_bf16(run_tp(cuda_lib, case, variant), oracle_tp(case))
+
+
+@functools.lru_cache(maxsize=1)
+def c_roofline():
+    return si.finalize_32768_tokens(weight_before_norm=False)
+
+
+@pytest.mark.parametrize("before", [False, True])
+def test_finalize_32768_tokens_full_size(cuda_lib, before):
+    # the bandwidth workload in the launch configuration the benchmark times
+    # (automatic choice), every output element against the oracle
+    case = c_roofline()
+    assert cuda_lib.select_finalize_variant(case.num_tokens) == "bulk_ring"
+    got = run_tp(cuda_lib, case, "auto", before=before)
+    stats = compare_bf16(got, oracle_tp(case, before=before))
+    assert stats["n"] == 32768 * 4096
+
+
+@functools.lru_cache(maxsize=1)
+def c_beam():
+    return si.beam_8000_live(poison_dead_rows=True)
+
+
+@pytest.mark.parametrize("variant", BEAM_VARIANTS)
+def test_beam_8000_live(cuda_lib, variant):
+    case = c_beam()
+    got = run_beam(cuda_lib, case, variant)
+    assert not np.isnan(bf16_bits_to_f64(got)).any(), "dead rows (NaN) leaked into the output"
+    compare_bf16(got, oracle_beam(case))
+
+
+# ---------------------------------------------------------------------------
+# edge cases: finalize + RMSNorm
+
+def small_case(T, *, stride=4096, wdt="fp32", seed=1, before=False, eps=1e-6):
+    return si.tp_case(f"edge_T{T}", T, indexed_rows=T * 8 + 3, row_stride=stride,
+                      invalid_frac=0.05, weights_dtype=wdt, seed=seed, weight_before_norm=before,
+                      eps=eps)
+
+
+@pytest.mark.parametrize("T", [2, 37, 65, 300, 1023, 1024, 1500])
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_ragged_token_counts(cuda_lib, T, variant):
+    case = small_case(T, seed=T, before=bool(T % 2), wdt="bf16" if T % 3 == 0 else "fp32")
+    compare_bf16(run_tp(cuda_lib, case, variant), oracle_tp(case))
+
+
+def test_ring_with_fewer_tokens_than_sms(cuda_lib):
+    case = small_case(5, seed=5)
+    compare_bf16(run_tp(cuda_lib, case, "bulk_ring"), oracle_tp(case))
+
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_zero_tokens_is_a_no_op(cuda_lib, variant):
+    case = small_case(3)
+    g = dev_bf16(case.gemm2)
+    out = torch.full((2, 4096), CANARY, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    cuda_lib.moe_finalize_rmsnorm(g, torch.empty((0, 8), device="cuda"),
+                                  torch.empty((0, 8), dtype=torch.int32, device="cuda"),
+                                  dev_bf16(case.norm_weight), out[:0], eps=1e-6, gain_center=1.0,
+                                  weight_before_norm=False, variant=variant)
+    torch.cuda.synchronize()
+    assert np.all(host_bits(out) == CANARY)
+
+
+def _special_index_case(before):
+    # tokens whose slots are all invalid, the boundary indices rows-1 / rows,
+    # INT32_MIN / INT32_MAX, duplicated indices and NaN weights on invalid slots
+    case = small_case(24, seed=7, before=before)
+    R = case.gemm2.shape[0]
+    idx = case.idx.copy()
+    w = case.weights.copy()
+    idx[0, :] = [-1, R, np.iinfo(np.int32).min, np.iinfo(np.int32).max, -7, R + 5, -1, R]
+    w[0, :] = np.nan
+    idx[1, :] = [R - 1, R, R - 1, -1, 0, 0, R + 1, 3]
+    w[1, 1] = w[1, 3] = w[1, 6] = np.nan
+    idx[2, :] = 5                                     # one row eight times
+    idx[3, :] = -1
+    idx[3, 7] = 11                                    # only the last slot valid
+    idx[4, :] = -1
+    idx[4, 0] = 12                                    # only the first slot valid
+    case.idx, case.weights = np.ascontiguousarray(idx), np.ascontiguousarray(w)
+    return case
+
+
+@pytest.mark.parametrize("before", [False, True])
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_special_indices(cuda_lib, variant, before):
+    case = _special_index_case(before)
+    got = run_tp(cuda_lib, case, variant)
+    assert np.all(bf16_bits_to_f64(got[0]) == 0.0)   # all-invalid token -> exact zeros
+    compare_bf16(got, oracle_tp(case))
+
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_all_invalid_with_zero_eps_gives_nan(cuda_lib, variant):
+    # the degenerate case of the formula: 0 * 1/sqrt(0); both sides give NaN
+    case = small_case(4, seed=8, eps=0.0)
+    case.idx[:] = -1
+    got = run_tp(cuda_lib, case, variant)
+    assert np.isnan(bf16_bits_to_f64(got)).all()
+    compare_bf16(got, oracle_tp(case))
+
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_no_rows_at_all(cuda_lib, variant):
+    # gemm2 with zero rows: every index is out of range
+    case = small_case(3, seed=9)
+    case.gemm2 = np.zeros((0, 4096), dtype=np.uint16)
+    got = run_tp(cuda_lib, case, variant)
+    assert np.all(bf16_bits_to_f64(got) == 0.0)
+
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_wide_row_stride(cuda_lib, variant):
+    case = si.tp_case("stride8192", 40, indexed_rows=400, padding_rows=9, row_stride=8192,
+                      invalid_frac=0.1, weights_dtype="fp32", seed=10, poison_padding=True)
+    got = run_tp(cuda_lib, case, variant)
+    compare_bf16(got, oracle_tp(case))
+
+
+@pytest.mark.parametrize("variant", ("token_cta", "bulk_ring"))
+def test_extreme_values(cuda_lib, variant):
+    # large magnitudes (sigma 1e15) and tiny ones (sigma 1e-15): the FP32
+    # reduction and the FP32 sum of squares stay finite and normal, and match
+    # (beyond |acc| ~ 2^57 the FP32 sum of squares of 4096 values overflows)
+    for sigma, seed in ((1e15, 11), (1e-15, 12)):
+        case = si.tp_case("extreme", 64, indexed_rows=512, sigma=sigma, invalid_frac=0.02,
+                          weights_dtype="fp32", seed=seed, eps=0.0)
+        compare_bf16(run_tp(cuda_lib, case, variant), oracle_tp(case))
+
+
+def test_non_default_stream(cuda_lib):
+    case = small_case(50, seed=13)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        got = run_tp(cuda_lib, case, "auto", stream=s)
+    compare_bf16(got, oracle_tp(case))
+
+
+def test_unsupported_hidden_raises(cuda_lib):
+    g = torch.zeros(16, 2048, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(cuda_lib.MoeFinalizeError) as e:
+        cuda_lib.moe_finalize_rmsnorm(g, torch.zeros(2, 8, device="cuda"),
+                                      torch.zeros(2, 8, dtype=torch.int32, device="cuda"),
+                                      torch.zeros(2048, dtype=torch.bfloat16, device="cuda"),
+                                      torch.zeros(2, 2048, dtype=torch.bfloat16, device="cuda"),
+                                      eps=1e-6, gain_center=1.0, weight_before_norm=False)
+    assert e.value.status == 5
+
+
+# ---------------------------------------------------------------------------
+# edge cases: Beam
+
+@pytest.mark.parametrize("K,H", [(1, 256), (32, 256), (8, 8192), (3, 7936), (5, 1536), (32, 8192),
+                                 (2, 2560), (8, 4096)])
+@pytest.mark.parametrize("variant", BEAM_VARIANTS)
+def test_beam_shapes(cuda_lib, K, H, variant):
+    case = si.beam_case(f"beam_{K}_{H}", 40, K, H, 37, routed_scale=2.5, seed=K * 1000 + H,
+                        poison_dead_rows=True)
+    compare_bf16(run_beam(cuda_lib, case, variant), oracle_beam(case))
+
+
+@pytest.mark.parametrize("variant", BEAM_VARIANTS)
+def test_beam_without_norm_is_bit_exact(cuda_lib, variant):
+    case = si.beam_case("beam_nonorm", 300, 8, 7168, 290, routed_scale=2.5, post_weight=False,
+                        post_eps=None, seed=21, poison_dead_rows=True)
+    got = run_beam(cuda_lib, case, variant)
+    assert np.array_equal(got, oracle_beam(case))
+
+
+@pytest.mark.parametrize("variant", BEAM_VARIANTS)
+def test_beam_unweighted_norm(cuda_lib, variant):
+    case = si.beam_case("beam_unweighted", 200, 4, 2048, 200, routed_scale=0.75,
+                        post_weight=False, post_eps=1e-5, seed=22)
+    compare_bf16(run_beam(cuda_lib, case, variant), oracle_beam(case))
+
+
+@pytest.mark.parametrize("live", [0, 1, 151, 152, 153, 1000])
+def test_beam_live_counts(cuda_lib, live):
+    case = si.beam_case("beam_live", 1000, 8, 1024, live, routed_scale=2.5, seed=23,
+                        poison_dead_rows=True)
+    got = run_beam(cuda_lib, case, "auto")
+    if live:
+        compare_bf16(got, oracle_beam(case))
+
+
+def test_beam_extra_weight_rows(cuda_lib):
+    case = si.beam_case("beam_wrows", 64, 8, 512, 10, routed_scale=1.0, seed=24)
+    compare_bf16(run_beam(cuda_lib, case, "bulk_ring"), oracle_beam(case))
+
+
+def test_beam_matches_tp_reduction_on_identity_map(cuda_lib):
+    # token-major rows with the identity route map: Beam without norm and scale
+    # 1 rounds the same FP32 sums that the tp path normalises; check the GPU
+    # Beam output against the Beam oracle and the tp GPU output against the
+    # tp oracle on the very same rows
+    cap, K, H = 64, 8, 4096
+    case = si.beam_case("beam_identity", cap, K, H, cap, routed_scale=1.0, post_weight=False,
+                        post_eps=None, seed=25)
+    assert np.array_equal(run_beam(cuda_lib, case, "bulk_ring"), oracle_beam(case))
+    tp = si.TpCase("identity", np.ascontiguousarray(case.expert_outputs.reshape(cap * K, H)),
+                   case.weights, np.arange(cap * K, dtype=np.int32).reshape(cap, K),
+                   np.zeros(H, dtype=np.uint16), H, 1e-6, 1.0, False)
+    compare_bf16(run_tp(cuda_lib, tp, "bulk_ring"), oracle_tp(tp))
+
+
+# ---------------------------------------------------------------------------
+# failure detection (a bounded wait that gives up; no fault, no hang)
+
+def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
+    assert cuda_lib.device_status(clear=True) == 0
+    cuda_lib.selftest_wait_timeout(20_000_000)        # 20 ms
+    assert cuda_lib.device_status(clear=False) == 7   # MF_ERR_DEVICE_TIMEOUT
+    assert cuda_lib.device_status(clear=True) == 7
+    assert cuda_lib.device_status(clear=True) == 0
+    case = small_case(8, seed=30)
+    compare_bf16(run_tp(cuda_lib, case, "bulk_ring"), oracle_tp(case))
