@@ -1,6 +1,9 @@
 """Comparison helpers for the tests (no finalize arithmetic here)."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 
 # Acceptance bar for every output element: |got - ref| <= 2^-7 * |ref| + 1e-6
@@ -42,6 +45,7 @@ def compare_bf16(got: np.ndarray, ref: np.ndarray, *, rel: float = REL_TOL, abs_
     # +0 and -0 compare equal as values; count them as exact matches
     exact |= (g == 0) & (r == 0)
     nan_r, nan_g = np.isnan(r), np.isnan(g)
+    exact |= nan_r & nan_g          # any NaN payload matches NaN
     assert np.array_equal(nan_r, nan_g), (
         f"NaN mismatch: ref NaN {int(nan_r.sum())}, got NaN {int(nan_g.sum())}, "
         f"first at {np.argwhere(nan_r != nan_g)[:4].tolist()}")
@@ -58,5 +62,9 @@ def compare_bf16(got: np.ndarray, ref: np.ndarray, *, rel: float = REL_TOL, abs_
         where = np.argwhere(bad)[:5]
         detail = [(tuple(int(i) for i in w), float(g[tuple(w)]), float(r[tuple(w)])) for w in where]
         raise AssertionError(f"{int(bad.sum())} elements outside the 1-ulp bound: {detail}")
+    log = os.environ.get("MF_PARITY_LOG")
+    if log:  # optional record of the per-test statistics
+        with open(log, "a") as f:
+            f.write(json.dumps({"test": os.environ.get("PYTEST_CURRENT_TEST", ""), **stats}) + "\n")
     assert stats["exact_frac"] >= min_exact, f"bit-exact fraction {stats['exact_frac']:.6f} < {min_exact}"
     return stats
