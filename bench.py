@@ -217,7 +217,7 @@ def make_tp_job(torch, mf, case: si.TpCase, device, variant: str, alternate: boo
                                 weight_before_norm=before, variant=variant)
 
     chosen = mf.select_finalize_variant(T) if variant == "auto" else variant
-    kernel = {"bulk_ring": "tp_ring_kernel", "token_cta": "tp_token_cta_kernel",
+    kernel = {"bulk": "tp_token_bulk_kernel", "token_cta": "tp_token_cta_kernel",
               "cluster": "tp_cluster_kernel"}[chosen]
     job = Job(case.name, T, si.algorithmic_bytes_tp(T, case.hidden, case.top_k, wbytes), kernel,
               launch, case, {"variant": chosen})
@@ -237,7 +237,7 @@ def make_beam_job(torch, mf, case: si.BeamCase, device, variant: str) -> Job:
         mf.beam_moe_finalize(xx, ww, oo, case.routed_scale, pp, case.post_eps, variant=variant)
 
     chosen = mf.select_beam_variant(case.live_tokens, K, H) if variant == "auto" else variant
-    kernel = {"bulk_ring": "beam_ring_kernel", "token_cta": "beam_token_cta_kernel"}[chosen]
+    kernel = {"bulk": "beam_token_bulk_kernel", "token_cta": "beam_token_cta_kernel"}[chosen]
     job = Job(case.name, case.live_tokens, si.algorithmic_bytes_beam(case.live_tokens, H, K),
               kernel, launch, case, {"variant": chosen})
     job.device_tensors = (x, w, pw, out)
@@ -520,8 +520,7 @@ def parse_args(argv=None):
     p.add_argument("--workload", default="roofline",
                    choices=("roofline", "padded", "beam", "small", "decode"))
     p.add_argument("--tokens", type=int, default=None, help="token count of --workload decode")
-    p.add_argument("--variant", default="auto", choices=("auto", "token_cta", "bulk_ring",
-                                                         "cluster"))
+    p.add_argument("--variant", default="auto", choices=("auto", "token_cta", "bulk", "cluster"))
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")

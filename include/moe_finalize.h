@@ -67,12 +67,13 @@ typedef enum mf_dtype {
 
 /* Kernel choice.  AUTO picks by size; the others force one kernel (for
  * validation and benchmarking, as the Beam wrappers' `strategy` argument
- * forces a path).  A variant that does not apply returns MF_ERR_INVALID. */
+ * forces a path).  Every variant computes the same result up to the order of
+ * the sum of squares.  A variant that does not apply returns MF_ERR_INVALID. */
 typedef enum mf_variant {
     MF_VARIANT_AUTO = 0,
     MF_VARIANT_TOKEN_CTA = 1,    /* one CTA per token, gathers held in registers */
-    MF_VARIANT_BULK_RING = 2,    /* persistent CTAs, bulk-copy ring of rows in shared memory */
-    MF_VARIANT_CLUSTER = 3       /* decode sizes: hidden split over a cluster, DSMEM reduction */
+    MF_VARIANT_BULK = 2,         /* one CTA per token, rows staged in shared memory by bulk copies */
+    MF_VARIANT_CLUSTER = 3       /* finalize+RMSNorm only: hidden split over a cluster, DSMEM reduction */
 } mf_variant;
 
 /*
@@ -168,7 +169,7 @@ mf_status beam_moe_finalize(const void *expert_outputs, int64_t capacity,
                             float routed_scale, const void *post_weight, float post_eps,
                             int has_post_norm, mf_stream_t stream);
 
-/* beam_moe_finalize with an explicit kernel choice (TOKEN_CTA or BULK_RING). */
+/* beam_moe_finalize with an explicit kernel choice (TOKEN_CTA or BULK). */
 mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity,
                                     const float *expert_weights, int64_t weight_rows,
                                     void *output, int64_t live_tokens, int32_t top_k,

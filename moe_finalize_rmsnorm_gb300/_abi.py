@@ -16,7 +16,7 @@ STATUS_NAMES = {
     5: "MF_ERR_UNSUPPORTED", 6: "MF_ERR_CUDA", 7: "MF_ERR_DEVICE_TIMEOUT", 8: "MF_ERR_INVALID",
 }
 MF_DTYPE_BF16, MF_DTYPE_FP32 = 0, 1
-VARIANTS = {"auto": 0, "token_cta": 1, "bulk_ring": 2, "cluster": 3}
+VARIANTS = {"auto": 0, "token_cta": 1, "bulk": 2, "cluster": 3}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
 # Every exported symbol with (restype, argtypes).

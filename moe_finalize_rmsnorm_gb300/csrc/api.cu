@@ -21,6 +21,7 @@ struct DeviceInfo {
     bool ready = false;
     int num_sms = 0;
     int smem_optin = 0;
+    int smem_per_sm = 0;
     unsigned *status = nullptr;  // device address of g_status_word
 };
 
@@ -38,10 +39,12 @@ mf_status device_info(const DeviceInfo **out) {
         if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
             cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
                 cudaSuccess ||
+            cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                   dev) != cudaSuccess ||
             cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status_word) !=
                 cudaSuccess ||
             mf::prepare_tp_kernels(d.smem_optin) != cudaSuccess ||
-            mf::prepare_beam_kernels(d.smem_optin) != cudaSuccess) {
+            mf::prepare_beam_kernels(d.smem_per_sm) != cudaSuccess) {
             (void)cudaGetLastError();
             return MF_ERR_CUDA;
         }
@@ -53,22 +56,17 @@ mf_status device_info(const DeviceInfo **out) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Token counts at or below this use the cluster decode kernel; above it and
-// below kRingMinTokens the one-CTA-per-token kernel.
-constexpr int64_t kClusterMaxTokens = 64;
-constexpr int64_t kRingMinTokens = 1024;
+// Finalize + RMSNorm: up to kClusterMaxTokens tokens the cluster kernel
+// spreads each token's gather over 8 SMs; above it one CTA per token.
+constexpr int64_t kClusterMaxTokens = 8;
 
 mf_variant pick_tp(int64_t num_tokens) {
     if (num_tokens <= 0) return MF_VARIANT_AUTO;
-    if (num_tokens <= kClusterMaxTokens) return MF_VARIANT_CLUSTER;
-    if (num_tokens < kRingMinTokens) return MF_VARIANT_TOKEN_CTA;
-    return MF_VARIANT_BULK_RING;
+    return num_tokens <= kClusterMaxTokens ? MF_VARIANT_CLUSTER : MF_VARIANT_TOKEN_CTA;
 }
 
-mf_variant pick_beam(int64_t live, int num_sms) {
-    if (live <= 0) return MF_VARIANT_AUTO;
-    return live >= num_sms ? MF_VARIANT_BULK_RING : MF_VARIANT_TOKEN_CTA;
-}
+// Beam: one CTA per live token with the token's block staged in shared memory.
+mf_variant pick_beam(int64_t live) { return live <= 0 ? MF_VARIANT_AUTO : MF_VARIANT_BULK; }
 
 mf_status from_launch(cudaError_t e) { return e == cudaSuccess ? MF_OK : MF_ERR_CUDA; }
 
@@ -141,8 +139,7 @@ mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
     switch (variant) {
         case MF_VARIANT_CLUSTER: return from_launch(mf::launch_tp_cluster(a, bf16w, s));
         case MF_VARIANT_TOKEN_CTA: return from_launch(mf::launch_tp_token_cta(a, bf16w, s));
-        case MF_VARIANT_BULK_RING:
-            return from_launch(mf::launch_tp_ring(a, bf16w, d->num_sms, d->smem_optin, s));
+        case MF_VARIANT_BULK: return from_launch(mf::launch_tp_bulk(a, bf16w, s));
         default: return MF_ERR_INVALID;
     }
 }
@@ -171,7 +168,7 @@ mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity
         return MF_ERR_SHAPE;
     if (post_weight && !has_post_norm) return MF_ERR_INVALID;
     if (variant != MF_VARIANT_AUTO && variant != MF_VARIANT_TOKEN_CTA &&
-        variant != MF_VARIANT_BULK_RING)
+        variant != MF_VARIANT_BULK)
         return MF_ERR_INVALID;
     if (live_tokens == 0) return MF_OK;
     if (!expert_outputs || !expert_weights || !output) return MF_ERR_NULL;
@@ -199,9 +196,8 @@ mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity
     a.timeout_ns = kWaitLimitNs;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    if (variant == MF_VARIANT_AUTO) variant = pick_beam(live_tokens, d->num_sms);
-    if (variant == MF_VARIANT_BULK_RING)
-        return from_launch(mf::launch_beam_ring(a, d->num_sms, d->smem_optin, s));
+    if (variant == MF_VARIANT_AUTO) variant = pick_beam(live_tokens);
+    if (variant == MF_VARIANT_BULK) return from_launch(mf::launch_beam_bulk(a, d->smem_per_sm, s));
     return from_launch(mf::launch_beam_token_cta(a, s));
 }
 
@@ -220,9 +216,7 @@ mf_variant mf_select_finalize_variant(int64_t num_tokens) { return pick_tp(num_t
 mf_variant mf_select_beam_variant(int64_t live_tokens, int32_t top_k, int32_t hidden) {
     (void)top_k;
     (void)hidden;
-    const DeviceInfo *d = nullptr;
-    if (device_info(&d) != MF_OK) return MF_VARIANT_AUTO;
-    return pick_beam(live_tokens, d->num_sms);
+    return pick_beam(live_tokens);
 }
 
 mf_status mf_device_status(int clear) {

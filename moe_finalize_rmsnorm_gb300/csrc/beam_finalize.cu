@@ -15,10 +15,10 @@
 //   beam_token_cta_kernel  one CTA per live token, H/8/CPT threads, each owning
 //                          CPT 16-byte chunks; slots are loaded in groups of 8
 //                          with every load of a group issued before its FMAs.
-//   beam_ring_kernel       persistent, one CTA per SM: a producer thread copies
-//                          each token's block in units of whole rows (<= 16 KB)
-//                          into a shared-memory ring with 1-D bulk copies;
-//                          consumer warps reduce, round, scale and normalise.
+//   beam_token_bulk_kernel one CTA per live token; thread 0 copies the token's
+//                          contiguous block into shared memory with 1-D bulk
+//                          copies on one mbarrier (two CTAs per SM), then
+//                          every thread reduces its chunks from shared memory.
 //
 // H ranges over 256..8192 in steps of 256 and K over 1..32, as the wrapper's
 // assertions allow.
@@ -144,159 +144,92 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
 }
 
 // ---------------------------------------------------------------------------
-// persistent bulk-copy ring
+// one CTA per live token, the token's rows staged in shared memory
 
-struct BeamRing {
-    int slots;
-    int rows_per_unit;
-    int unit_bytes;
-    size_t bytes;
-    size_t full, empty, redbar, red;
-};
-
-__host__ __device__ inline BeamRing beam_ring_layout(int slots, int rows_per_unit, int hidden) {
-    BeamRing L;
-    L.slots = slots;
-    L.rows_per_unit = rows_per_unit;
-    L.unit_bytes = rows_per_unit * hidden * 2;
-    size_t off = static_cast<size_t>(slots) * L.unit_bytes;
-    L.full = off;   off += sizeof(uint64_t) * slots;
-    L.empty = off;  off += sizeof(uint64_t) * slots;
-    L.redbar = off; off += sizeof(uint64_t) * 2;
-    L.red = off;    off += sizeof(float) * 2 * 32;
-    L.bytes = off;
-    return L;
-}
-
-constexpr int kMaxUnitBytes = 16384;
-
+// A token's K rows are contiguous, so thread 0 moves them with one bulk copy
+// per piece (as many whole rows as fit half an SM's shared memory: all 8 rows,
+// 114,688 B, at H = 7168), completing on one mbarrier.  Data in flight holds
+// no registers, and two CTAs per SM keep two tokens' blocks in flight while
+// one of them reduces.  Rows beyond one piece are copied piece by piece into
+// the same buffer.
 template <int CPT>
-__global__ void __launch_bounds__(beam_max_threads<CPT>() == 1024 ? 1024 : beam_max_threads<CPT>() + 32, 1)
-    beam_ring_kernel(const BeamArgs a, const int slots, const int rows_per_unit) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int H = a.hidden, K = a.top_k;
-    const BeamRing L = beam_ring_layout(slots, rows_per_unit, H);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
-    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
-    uint64_t *redbar = reinterpret_cast<uint64_t *>(smem + L.redbar);
-    float *red = reinterpret_cast<float *>(smem + L.red);
-    const uint32_t ring_base = smem_u32(smem);
-
-    const int NC = blockDim.x - 32;
-    const int NCW = NC >> 5;
+__global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
+    beam_token_bulk_kernel(const BeamArgs a, const int rows_per_piece) {
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    __shared__ uint64_t bar;
+    __shared__ float red[32];
+    __shared__ float wsm[32];
+    const int NT = blockDim.x;
     const int tid = threadIdx.x;
+    const int64_t t = blockIdx.x;
+    const int K = a.top_k, H = a.hidden;
+    const uint32_t row_bytes = static_cast<uint32_t>(H) * 2;
+    const uint32_t base = smem_u32(rows_smem);
+    const uint32_t bar_addr = smem_u32(&bar);
+    const uint16_t *xt = a.x + t * K * static_cast<int64_t>(H);
+
     if (tid == 0) {
-        for (int s = 0; s < slots; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), NCW);
-        }
-        mbar_init(smem_u32(&redbar[0]), NCW);
-        mbar_init(smem_u32(&redbar[1]), NCW);
+        mbar_init(bar_addr, 1);
         fence_mbar_init();
     }
+    if (tid < K) wsm[tid] = __ldg(a.weights + t * K + tid);
     __syncthreads();
 
-    const int64_t T = a.live;
-    const int64_t stride = gridDim.x;
-    const int units = K / rows_per_unit;
-    const int64_t token_elems = static_cast<int64_t>(K) * H;
+    float acc[CPT][8];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[c][j] = 0.f;
 
-    if (tid >= NC) {
-        // ------------------------------------------------------ producer
-        if (tid != NC) return;
-        const uint64_t policy = policy_evict_first();
-        uint32_t pos = 0;
-        bool ok = true;
-        for (int64_t t = blockIdx.x; t < T && ok; t += stride) {
-            const uint16_t *src = a.x + t * token_elems;
-            for (int u = 0; u < units; ++u) {
-                const int s = pos % slots;
-                const uint32_t ph = (pos / slots) & 1u;
-                if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, a.timeout_ns)) { ok = false; break; }
-                const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, L.unit_bytes);
-                bulk_copy_g2s_hint(ring_base + static_cast<uint32_t>(s) * L.unit_bytes,
-                                   src + static_cast<int64_t>(u) * rows_per_unit * H, L.unit_bytes,
-                                   fb, policy);
-                ++pos;
-            }
+    bool ok = true;
+    uint32_t phase = 0;
+    for (int k0 = 0; k0 < K; k0 += rows_per_piece, phase ^= 1u) {
+        const int n = K - k0 < rows_per_piece ? K - k0 : rows_per_piece;
+        if (tid == 0) {
+            if (k0 > 0) fence_proxy_async_smem();  // earlier reads of the buffer come first
+            mbar_arrive_expect_tx(bar_addr, n * row_bytes);
+            bulk_copy_g2s_hint(base, xt + static_cast<int64_t>(k0) * H, n * row_bytes, bar_addr,
+                               policy_evict_first());
         }
-        if (!ok) {
+        if (!mbar_wait(bar_addr, phase, a.timeout_ns)) {
             atomicOr(a.status, kStatusWaitTimeout);
-            const uint32_t first = pos > static_cast<uint32_t>(slots) ? pos - slots : 0u;
-            for (uint32_t p = first; p < pos; ++p)
-                (void)mbar_wait(smem_u32(&full[p % slots]), (p / slots) & 1u, a.timeout_ns);
+            ok = false;
+            (void)mbar_wait(bar_addr, phase, a.timeout_ns);  // let the copy land before exit
         }
-        return;
+        for (int r = 0; r < n; ++r) {
+            const float w = wsm[k0 + r];
+            const uint32_t row = base + static_cast<uint32_t>(r) * row_bytes;
+            uint4 q[CPT];
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) q[c] = lds_16(row + (tid + c * NT) * kChunkBytes);
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) {
+                float x[8];
+                unpack8(q[c], x);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[c][j] = __fmaf_rn(w, x[j], acc[c][j]);
+            }
+        }
+        if (k0 + rows_per_piece < K) __syncthreads();  // the next piece reuses the buffer
     }
 
-    // ---------------------------------------------------------- consumers
-    const int lane = tid & 31, warp = tid >> 5;
+    round_scale_round<CPT>(acc, a.routed_scale);
     const bool norm = a.has_norm != 0;
-    uint32_t pos = 0, titer = 0;
-    int64_t t = blockIdx.x;
-    // lane k holds w[t, k]; the next token's weights are fetched one token ahead
-    float wnext = (t < T && lane < K) ? __ldg(a.weights + t * K + lane) : 0.f;
-    for (; t < T; t += stride, ++titer) {
-        const float wl = wnext;
-        if (t + stride < T && lane < K) wnext = __ldg(a.weights + (t + stride) * K + lane);
-
-        float acc[CPT][8];
-#pragma unroll
-        for (int c = 0; c < CPT; ++c)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[c][j] = 0.f;
-
-        for (int u = 0; u < units; ++u) {
-            const int s = pos % slots;
-            const uint32_t ph = (pos / slots) & 1u;
-            if (!mbar_wait(smem_u32(&full[s]), ph, a.timeout_ns)) {
-                atomicOr(a.status, kStatusWaitTimeout);
-                return;
-            }
-            const uint32_t slot = ring_base + static_cast<uint32_t>(s) * L.unit_bytes;
-            for (int r = 0; r < rows_per_unit; ++r) {
-                const float w = __shfl_sync(0xffffffffu, wl, u * rows_per_unit + r);
-                const uint32_t row = slot + static_cast<uint32_t>(r) * H * 2;
-                uint4 q[CPT];
-#pragma unroll
-                for (int c = 0; c < CPT; ++c) q[c] = lds_16(row + (tid + c * NC) * kChunkBytes);
-#pragma unroll
-                for (int c = 0; c < CPT; ++c) {
-                    float x[8];
-                    unpack8(q[c], x);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[c][j] = __fmaf_rn(w, x[j], acc[c][j]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-            ++pos;
-        }
-
-        round_scale_round<CPT>(acc, a.routed_scale);
-        float rs = 1.f;
-        if (norm) {
-            const float ss = warp_sum(sum_squares<CPT>(acc));
-            const int b = titer & 1;
-            if (lane == 0) {
-                red[b * 32 + warp] = ss;
-                mbar_arrive(smem_u32(&redbar[b]));
-            }
-            if (!mbar_wait(smem_u32(&redbar[b]), (titer >> 1) & 1u, a.timeout_ns)) {
-                atomicOr(a.status, kStatusWaitTimeout);
-                return;
-            }
-            float tot = 0.f;
-            for (int i = 0; i < NCW; ++i) tot += red[b * 32 + i];
-            rs = inv_rms(tot, H, a.post_eps);
-        }
-        beam_store<CPT>(acc, a, norm, rs, a.out + t * H, tid, NC);
+    float rs = 1.f;
+    if (norm) {
+        const float ss = warp_sum(sum_squares<CPT>(acc));
+        if ((tid & 31) == 0) red[tid >> 5] = ss;
+        __syncthreads();
+        float tot = 0.f;
+        const int nw = NT >> 5;
+        for (int i = 0; i < nw; ++i) tot += red[i];
+        rs = inv_rms(tot, H, a.post_eps);
     }
+    if (ok) beam_store<CPT>(acc, a, norm, rs, a.out + t * H, tid, NT);
 }
 
-// Chunks per thread: the largest of 4, 2, 1 that divides H/256 and leaves at
-// least 128 threads (a multiple of 32 either way).
+// Chunks per thread of the register kernel: the largest of 4, 2, 1 that
+// divides H/256 and leaves at least 128 threads (a multiple of 32 either way).
 int beam_cpt(int hidden) {
     const int groups = hidden / 256;
     for (int cpt : {4, 2})
@@ -304,19 +237,20 @@ int beam_cpt(int hidden) {
     return 1;
 }
 
-// Whole rows per ring unit: the largest divisor of K whose rows fit 16 KB.
-int beam_rows_per_unit(int top_k, int hidden) {
-    for (int r = top_k; r > 1; --r)
-        if (top_k % r == 0 && r * hidden * 2 <= kMaxUnitBytes) return r;
-    return 1;
+// Chunks per thread of the staged kernel: 2 when that leaves at least 256
+// threads, else 1.
+int beam_bulk_cpt(int hidden) {
+    return ((hidden / 256) % 2 == 0 && hidden / 16 >= 256) ? 2 : 1;
 }
 
-int beam_slots(int smem_optin, int rows_per_unit, int hidden) {
-    int slots = 1;
-    while (beam_ring_layout(slots + 1, rows_per_unit, hidden).bytes <=
-           static_cast<size_t>(smem_optin))
-        ++slots;
-    return slots;
+// Shared memory one staged CTA may use so that two fit on an SM (each CTA
+// also takes 1 KB reserved by the system and a few hundred bytes of static
+// shared memory).
+int beam_bulk_budget(int smem_per_sm) { return smem_per_sm / 2 - 1024 - 512; }
+
+int beam_bulk_rows(int smem_per_sm, int top_k, int hidden) {
+    const int rows = beam_bulk_budget(smem_per_sm) / (hidden * 2);
+    return rows < 1 ? 1 : (rows > top_k ? top_k : rows);
 }
 
 __global__ void wait_timeout_selftest_kernel(unsigned *status, uint64_t timeout_ns) {
@@ -333,15 +267,13 @@ __global__ void wait_timeout_selftest_kernel(unsigned *status, uint64_t timeout_
 
 }  // namespace
 
-cudaError_t prepare_beam_kernels(int smem_optin) {
-    cudaError_t e = cudaFuncSetAttribute(beam_ring_kernel<1>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin);
+cudaError_t prepare_beam_kernels(int smem_per_sm) {
+    const int budget = beam_bulk_budget(smem_per_sm);
+    cudaError_t e = cudaFuncSetAttribute(beam_token_bulk_kernel<1>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(beam_ring_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_optin);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(beam_ring_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem_optin);
+        e = cudaFuncSetAttribute(beam_token_bulk_kernel<2>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
     return e;
 }
 
@@ -356,18 +288,15 @@ cudaError_t launch_beam_token_cta(const BeamArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_beam_ring(const BeamArgs &a, int num_sms, int smem_optin, cudaStream_t s) {
-    const int cpt = beam_cpt(a.hidden);
-    const int rpu = beam_rows_per_unit(a.top_k, a.hidden);
-    const int slots = beam_slots(smem_optin, rpu, a.hidden);
-    const size_t bytes = beam_ring_layout(slots, rpu, a.hidden).bytes;
-    const int64_t grid = a.live < num_sms ? a.live : num_sms;
-    const dim3 block(a.hidden / 8 / cpt + 32);
-    switch (cpt) {
-        case 4: beam_ring_kernel<4><<<static_cast<unsigned>(grid), block, bytes, s>>>(a, slots, rpu); break;
-        case 2: beam_ring_kernel<2><<<static_cast<unsigned>(grid), block, bytes, s>>>(a, slots, rpu); break;
-        default: beam_ring_kernel<1><<<static_cast<unsigned>(grid), block, bytes, s>>>(a, slots, rpu); break;
-    }
+cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, cudaStream_t s) {
+    const int cpt = beam_bulk_cpt(a.hidden);
+    const int rows = beam_bulk_rows(smem_per_sm, a.top_k, a.hidden);
+    const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;
+    const dim3 grid(static_cast<unsigned>(a.live)), block(a.hidden / 8 / cpt);
+    if (cpt == 2)
+        beam_token_bulk_kernel<2><<<grid, block, bytes, s>>>(a, rows);
+    else
+        beam_token_bulk_kernel<1><<<grid, block, bytes, s>>>(a, rows);
     return cudaGetLastError();
 }
 

@@ -123,6 +123,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
     }
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses (and, after
+// a CTA barrier, the other threads') before later bulk-copy writes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // One-dimensional bulk copy global -> this CTA's shared memory, completing
 // `bytes` of transaction count on mbarrier `bar`.  Both addresses 16-byte
 // aligned, bytes a multiple of 16.

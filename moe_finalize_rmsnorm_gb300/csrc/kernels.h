@@ -44,17 +44,17 @@ struct BeamArgs {
 };
 
 // Per-device one-time set-up (kernel attributes).  `smem_optin` is the
-// device's opt-in shared memory per block.
+// device's opt-in shared memory per block, `smem_per_sm` its shared memory
+// per multiprocessor.
 cudaError_t prepare_tp_kernels(int smem_optin);
-cudaError_t prepare_beam_kernels(int smem_optin);
+cudaError_t prepare_beam_kernels(int smem_per_sm);
 
 cudaError_t launch_tp_token_cta(const TpArgs &a, bool bf16_weights, cudaStream_t s);
 cudaError_t launch_tp_cluster(const TpArgs &a, bool bf16_weights, cudaStream_t s);
-cudaError_t launch_tp_ring(const TpArgs &a, bool bf16_weights, int num_sms, int smem_optin,
-                           cudaStream_t s);
+cudaError_t launch_tp_bulk(const TpArgs &a, bool bf16_weights, cudaStream_t s);
 
 cudaError_t launch_beam_token_cta(const BeamArgs &a, cudaStream_t s);
-cudaError_t launch_beam_ring(const BeamArgs &a, int num_sms, int smem_optin, cudaStream_t s);
+cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, cudaStream_t s);
 
 cudaError_t launch_wait_timeout_selftest(unsigned *status, uint64_t timeout_ns, cudaStream_t s);
 

@@ -20,14 +20,11 @@
 //                        CTA owning 4096/C columns; the partial sums of
 //                        squares are exchanged through distributed shared
 //                        memory, so a token's 64 KB gather spreads over C SMs.
-//   tp_ring_kernel       persistent, one CTA per SM: a producer thread streams
-//                        the valid rows of the CTA's tokens into a ring of
-//                        8 KB shared-memory slots with 1-D bulk copies
-//                        (cp.async.bulk, completion on per-slot mbarriers);
-//                        consumer warps read each slot once, FMA into FP32
-//                        registers, release the slot, and finish each token
-//                        with the RMSNorm epilogue and 16-byte streaming stores.
-//                        Up to ~28 rows (224 KB) are in flight per SM.
+//   tp_token_bulk_kernel one CTA per token; thread 0 stages the token's valid
+//                        rows in shared memory with 1-D bulk copies
+//                        (cp.async.bulk) completing on one mbarrier, so no
+//                        registers are held by data in flight and three
+//                        CTAs (192 KB of rows) fit per SM.
 //
 // Every wait on an mbarrier is bounded (TpArgs::timeout_ns); a wait that gives
 // up ORs kStatusWaitTimeout into the device status word and the kernel returns.
@@ -39,8 +36,6 @@ namespace mf {
 namespace {
 
 constexpr int kChunksPerRow = kTpHidden / kChunkElems;  // 512
-constexpr uint32_t kMetaLast = 1u;   // slot holds the token's last valid row
-constexpr uint32_t kMetaEmpty = 2u;  // token has no valid row; slot carries no data
 
 // Load the 8 route entries of token t (same address across the block: the
 // loads are broadcasts).
@@ -233,200 +228,101 @@ __global__ void __launch_bounds__(kChunksPerRow / C) tp_cluster_kernel(const TpA
 }
 
 // ---------------------------------------------------------------------------
-// persistent bulk-copy ring
+// one CTA per token, rows staged in shared memory by bulk copies
 
-struct RingMeta {
-    float w;
-    uint32_t flags;
-};
+// Thread 0 copies every valid row of the token (8 KB each) into its slot of a
+// 64 KB shared-memory buffer with one-dimensional bulk copies that complete on
+// a single mbarrier; the data in flight holds no registers, so three CTAs
+// (192 KB of rows) can be in flight per SM.  Every thread then waits on the
+// barrier, reads its CPT chunks of each valid row from shared memory and runs
+// the same FMA chain and epilogue as the register kernel.
+constexpr int kBulkCPT = 2;                      // 256 threads
+constexpr int kBulkThreads = kChunksPerRow / kBulkCPT;
+constexpr int kBulkSmem = kTpTopK * kTpRowBytes;  // 64 KB of rows
 
-struct RingLayout {
-    int slots;
-    size_t bytes;
-    // offsets from the dynamic shared memory base
-    size_t full, empty, redbar, meta, red;
-};
+template <bool BF16W>
+__global__ void __launch_bounds__(kBulkThreads)
+    tp_token_bulk_kernel(const TpArgs a) {
+    constexpr int NT = kBulkThreads, NW = NT / 32, CPT = kBulkCPT;
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    __shared__ uint64_t bar;
+    __shared__ float red[NW];
 
-__host__ __device__ inline RingLayout ring_layout(int slots, int slot_bytes, int consumer_warps) {
-    RingLayout L;
-    L.slots = slots;
-    size_t off = static_cast<size_t>(slots) * slot_bytes;
-    L.full = off;   off += sizeof(uint64_t) * slots;
-    L.empty = off;  off += sizeof(uint64_t) * slots;
-    L.redbar = off; off += sizeof(uint64_t) * 2;
-    L.meta = off;   off += sizeof(RingMeta) * slots;
-    L.red = off;    off += sizeof(float) * 2 * consumer_warps;
-    L.bytes = off;
-    return L;
-}
-
-template <int CPT, bool BF16W>
-__global__ void __launch_bounds__(kChunksPerRow / CPT + 32, 1)
-    tp_ring_kernel(const TpArgs a, const int slots) {
-    constexpr int NC = kChunksPerRow / CPT;  // consumer threads
-    constexpr int NCW = NC / 32;
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const RingLayout L = ring_layout(slots, kTpRowBytes, NCW);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.full);
-    uint64_t *empty = reinterpret_cast<uint64_t *>(smem + L.empty);
-    uint64_t *redbar = reinterpret_cast<uint64_t *>(smem + L.redbar);
-    RingMeta *meta = reinterpret_cast<RingMeta *>(smem + L.meta);
-    float *red = reinterpret_cast<float *>(smem + L.red);
-    const uint32_t ring_base = smem_u32(smem);
-
+    const int64_t t = blockIdx.x;
     const int tid = threadIdx.x;
+    const uint32_t rows_base = smem_u32(rows_smem);
+    const uint32_t bar_addr = smem_u32(&bar);
+
+    int idx[8];
+    float w[8];
+    load_route<BF16W>(a, t, idx, w);
+    uint32_t mask = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mask |= (slot_valid(idx[k], a.rows) ? 1u : 0u) << k;
+
     if (tid == 0) {
-        for (int s = 0; s < slots; ++s) {
-            mbar_init(smem_u32(&full[s]), 1);
-            mbar_init(smem_u32(&empty[s]), NCW);
-        }
-        mbar_init(smem_u32(&redbar[0]), NCW);
-        mbar_init(smem_u32(&redbar[1]), NCW);
+        mbar_init(bar_addr, 1);
         fence_mbar_init();
-    }
-    __syncthreads();
-
-    const int64_t T = a.num_tokens;
-    const int64_t stride = gridDim.x;
-
-    if (tid >= NC) {
-        // ------------------------------------------------------ producer
-        if (tid != NC) return;
         const uint64_t policy = policy_evict_first();
-        uint32_t pos = 0;
-        int64_t t = blockIdx.x;
-        if (t >= T) return;
-        int nidx[8];
-        float nw[8];
-        load_route<BF16W>(a, t, nidx, nw);
-        bool ok = true;
-        for (; t < T && ok; t += stride) {
-            int idx[8];
-            float w[8];
+        mbar_arrive_expect_tx(bar_addr, static_cast<uint32_t>(__popc(mask)) * kTpRowBytes);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) { idx[k] = nidx[k]; w[k] = nw[k]; }
-            if (t + stride < T) load_route<BF16W>(a, t + stride, nidx, nw);  // prefetch
-            uint32_t mask = 0;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) mask |= (slot_valid(idx[k], a.rows) ? 1u : 0u) << k;
-            if (mask == 0) {
-                const int s = pos % slots;
-                const uint32_t ph = (pos / slots) & 1u;
-                if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, a.timeout_ns)) { ok = false; break; }
-                meta[s] = RingMeta{0.f, kMetaLast | kMetaEmpty};
-                mbar_arrive(smem_u32(&full[s]));
-                ++pos;
-                continue;
-            }
-            const int last = 31 - __clz(mask);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (!((mask >> k) & 1u)) continue;
-                const int s = pos % slots;
-                const uint32_t ph = (pos / slots) & 1u;
-                if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, a.timeout_ns)) { ok = false; break; }
-                meta[s] = RingMeta{w[k], k == last ? kMetaLast : 0u};
-                const uint32_t fb = smem_u32(&full[s]);
-                mbar_arrive_expect_tx(fb, kTpRowBytes);
-                bulk_copy_g2s_hint(ring_base + static_cast<uint32_t>(s) * kTpRowBytes,
-                                   a.gemm2 + static_cast<int64_t>(idx[k]) * a.ld, kTpRowBytes, fb,
-                                   policy);
-                ++pos;
-            }
-        }
-        if (!ok) {
-            atomicOr(a.status, kStatusWaitTimeout);
-            // drain: wait (bounded) for the copies this thread issued
-            const uint32_t first = pos > static_cast<uint32_t>(slots) ? pos - slots : 0u;
-            for (uint32_t p = first; p < pos; ++p)
-                (void)mbar_wait(smem_u32(&full[p % slots]), (p / slots) & 1u, a.timeout_ns);
-        }
-        return;
+        for (int k = 0; k < 8; ++k)
+            if ((mask >> k) & 1u)
+                bulk_copy_g2s_hint(rows_base + k * kTpRowBytes,
+                                   a.gemm2 + static_cast<int64_t>(idx[k]) * a.ld, kTpRowBytes,
+                                   bar_addr, policy);
     }
-
-    // ---------------------------------------------------------- consumers
-    const int lane = tid & 31, warp = tid >> 5;
     float g[CPT][8];
 #pragma unroll
-    for (int c = 0; c < CPT; ++c) load_gain(a, tid + c * NC, g[c]);
-    const bool before = a.before != 0;
+    for (int c = 0; c < CPT; ++c) load_gain(a, tid + c * NT, g[c]);
+    __syncthreads();  // the barrier is initialised before anyone waits on it
 
-    uint32_t pos = 0, titer = 0;
-    for (int64_t t = blockIdx.x; t < T; t += stride, ++titer) {
-        float acc[CPT][8];
-#pragma unroll
-        for (int c = 0; c < CPT; ++c)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) acc[c][j] = 0.f;
-
-        for (;;) {
-            const int s = pos % slots;
-            const uint32_t ph = (pos / slots) & 1u;
-            if (!mbar_wait(smem_u32(&full[s]), ph, a.timeout_ns)) {
-                atomicOr(a.status, kStatusWaitTimeout);
-                return;
-            }
-            const RingMeta m = meta[s];
-            if (!(m.flags & kMetaEmpty)) {
-                const uint32_t slot = ring_base + static_cast<uint32_t>(s) * kTpRowBytes;
-                uint4 q[CPT];
-#pragma unroll
-                for (int c = 0; c < CPT; ++c) q[c] = lds_16(slot + (tid + c * NC) * kChunkBytes);
-#pragma unroll
-                for (int c = 0; c < CPT; ++c) {
-                    float x[8];
-                    unpack8(q[c], x);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[c][j] = __fmaf_rn(m.w, x[j], acc[c][j]);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-            ++pos;
-            if (m.flags & kMetaLast) break;
-        }
-
-        const float ss = warp_sum(prenorm<CPT>(acc, g, before));
-        const int b = titer & 1;
-        if (lane == 0) {
-            red[b * NCW + warp] = ss;
-            mbar_arrive(smem_u32(&redbar[b]));
-        }
-        if (!mbar_wait(smem_u32(&redbar[b]), (titer >> 1) & 1u, a.timeout_ns)) {
-            atomicOr(a.status, kStatusWaitTimeout);
-            return;
-        }
-        float tot = 0.f;
-#pragma unroll
-        for (int i = 0; i < NCW; ++i) tot += red[b * NCW + i];
-        const float r = rsqrtf(__fmaf_rn(tot, 1.0f / kTpHidden, a.eps));
-        scale_store<CPT, NC>(acc, g, before, r, a.out + t * kTpHidden, tid);
+    bool ok = mbar_wait(bar_addr, 0u, a.timeout_ns);
+    if (!ok) {
+        atomicOr(a.status, kStatusWaitTimeout);
+        ok = mbar_wait(bar_addr, 0u, a.timeout_ns);  // let copies in flight land before exit
     }
-}
 
-constexpr int kRingCPT = 2;  // 256 consumer threads + 1 producer warp
+    float acc[CPT][8];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[c][j] = 0.f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (!((mask >> k) & 1u)) continue;
+        uint4 q[CPT];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) q[c] = lds_16(rows_base + k * kTpRowBytes + (tid + c * NT) * kChunkBytes);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+            float x[8];
+            unpack8(q[c], x);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[c][j] = __fmaf_rn(w[k], x[j], acc[c][j]);
+        }
+    }
 
-int ring_slots(int smem_optin) {
-    const int ncw = kChunksPerRow / kRingCPT / 32;
-    int slots = 1;
-    while (ring_layout(slots + 1, kTpRowBytes, ncw).bytes <= static_cast<size_t>(smem_optin))
-        ++slots;
-    return slots;
-}
-
-template <typename K>
-cudaError_t set_smem(K kernel, size_t bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(bytes));
+    const bool before = a.before != 0;
+    const float ss = warp_sum(prenorm<CPT>(acc, g, before));
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < NW; ++i) tot += red[i];
+    const float r = rsqrtf(__fmaf_rn(tot, 1.0f / kTpHidden, a.eps));
+    if (ok) scale_store<CPT, NT>(acc, g, before, r, a.out + t * kTpHidden, tid);
 }
 
 }  // namespace
 
 cudaError_t prepare_tp_kernels(int smem_optin) {
-    const int slots = ring_slots(smem_optin);
-    const size_t bytes = ring_layout(slots, kTpRowBytes, kChunksPerRow / kRingCPT / 32).bytes;
-    cudaError_t e = set_smem(tp_ring_kernel<kRingCPT, false>, bytes);
-    if (e == cudaSuccess) e = set_smem(tp_ring_kernel<kRingCPT, true>, bytes);
+    (void)smem_optin;
+    cudaError_t e = cudaFuncSetAttribute(tp_token_bulk_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tp_token_bulk_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(tp_cluster_kernel<16, false>,
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -468,16 +364,12 @@ cudaError_t launch_tp_cluster(const TpArgs &a, bool bf16_weights, cudaStream_t s
     return launch_cluster_c<8>(a, bf16_weights, s);
 }
 
-cudaError_t launch_tp_ring(const TpArgs &a, bool bf16_weights, int num_sms, int smem_optin,
-                           cudaStream_t s) {
-    const int slots = ring_slots(smem_optin);
-    const size_t bytes = ring_layout(slots, kTpRowBytes, kChunksPerRow / kRingCPT / 32).bytes;
-    const int64_t grid = a.num_tokens < num_sms ? a.num_tokens : num_sms;
-    const dim3 block(kChunksPerRow / kRingCPT + 32);
+cudaError_t launch_tp_bulk(const TpArgs &a, bool bf16_weights, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(kBulkThreads);
     if (bf16_weights)
-        tp_ring_kernel<kRingCPT, true><<<static_cast<unsigned>(grid), block, bytes, s>>>(a, slots);
+        tp_token_bulk_kernel<true><<<grid, block, kBulkSmem, s>>>(a);
     else
-        tp_ring_kernel<kRingCPT, false><<<static_cast<unsigned>(grid), block, bytes, s>>>(a, slots);
+        tp_token_bulk_kernel<false><<<grid, block, kBulkSmem, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -66,10 +66,10 @@ def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
     d = bench.source_digest()
     (tmp_path / "k.md").write_text(
-        f"traffic: kernel=tp_ring_kernel workload=w bytes_per_launch=123 sources={d}\n"
-        "traffic: kernel=tp_ring_kernel workload=v bytes_per_launch=9 sources=stale\n")
-    assert bench.recorded_traffic("tp_ring_kernel", "w") == 123
-    assert bench.recorded_traffic("tp_ring_kernel", "v") is None
+        f"traffic: kernel=tp_token_cta_kernel workload=w bytes_per_launch=123 sources={d}\n"
+        "traffic: kernel=tp_token_cta_kernel workload=v bytes_per_launch=9 sources=stale\n")
+    assert bench.recorded_traffic("tp_token_cta_kernel", "w") == 123
+    assert bench.recorded_traffic("tp_token_cta_kernel", "v") is None
     assert bench.recorded_traffic("other", "w") is None
 
 

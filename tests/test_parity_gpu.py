@@ -18,8 +18,8 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 CANARY = 0x1234
-TP_VARIANTS = ("cluster", "token_cta", "bulk_ring", "auto")
-BEAM_VARIANTS = ("token_cta", "bulk_ring", "auto")
+TP_VARIANTS = ("cluster", "token_cta", "bulk", "auto")
+BEAM_VARIANTS = ("token_cta", "bulk", "auto")
 
 
 @pytest.fixture(scope="session", autouse=True)
@@ -140,7 +140,7 @@ def test_finalize_32768_tokens_full_size(cuda_lib, before):
     # the bandwidth workload in the launch configuration the benchmark times
     # (automatic choice), every output element against the oracle
     case = c_roofline()
-    assert cuda_lib.select_finalize_variant(case.num_tokens) == "bulk_ring"
+    assert cuda_lib.select_finalize_variant(case.num_tokens) == "token_cta"
     got = run_tp(cuda_lib, case, "auto", before=before)
     stats = compare_bf16(got, oracle_tp(case, before=before))
     assert stats["n"] == 32768 * 4096
@@ -175,9 +175,10 @@ def test_ragged_token_counts(cuda_lib, T, variant):
     compare_bf16(run_tp(cuda_lib, case, variant), oracle_tp(case))
 
 
-def test_ring_with_fewer_tokens_than_sms(cuda_lib):
+def test_fewer_tokens_than_sms(cuda_lib):
     case = small_case(5, seed=5)
-    compare_bf16(run_tp(cuda_lib, case, "bulk_ring"), oracle_tp(case))
+    for v in ("bulk", "token_cta", "cluster"):
+        compare_bf16(run_tp(cuda_lib, case, v), oracle_tp(case))
 
 
 @pytest.mark.parametrize("variant", TP_VARIANTS)
@@ -249,7 +250,7 @@ def test_wide_row_stride(cuda_lib, variant):
     compare_bf16(got, oracle_tp(case))
 
 
-@pytest.mark.parametrize("variant", ("token_cta", "bulk_ring"))
+@pytest.mark.parametrize("variant", ("token_cta", "bulk"))
 def test_extreme_values(cuda_lib, variant):
     # large magnitudes (sigma 1e15) and tiny ones (sigma 1e-15): the FP32
     # reduction and the FP32 sum of squares stay finite and normal, and match
@@ -317,7 +318,7 @@ def test_beam_live_counts(cuda_lib, live):
 
 def test_beam_extra_weight_rows(cuda_lib):
     case = si.beam_case("beam_wrows", 64, 8, 512, 10, routed_scale=1.0, seed=24)
-    compare_bf16(run_beam(cuda_lib, case, "bulk_ring"), oracle_beam(case))
+    compare_bf16(run_beam(cuda_lib, case, "bulk"), oracle_beam(case))
 
 
 def test_beam_matches_tp_reduction_on_identity_map(cuda_lib):
@@ -328,11 +329,11 @@ def test_beam_matches_tp_reduction_on_identity_map(cuda_lib):
     cap, K, H = 64, 8, 4096
     case = si.beam_case("beam_identity", cap, K, H, cap, routed_scale=1.0, post_weight=False,
                         post_eps=None, seed=25)
-    assert np.array_equal(run_beam(cuda_lib, case, "bulk_ring"), oracle_beam(case))
+    assert np.array_equal(run_beam(cuda_lib, case, "bulk"), oracle_beam(case))
     tp = si.TpCase("identity", np.ascontiguousarray(case.expert_outputs.reshape(cap * K, H)),
                    case.weights, np.arange(cap * K, dtype=np.int32).reshape(cap, K),
                    np.zeros(H, dtype=np.uint16), H, 1e-6, 1.0, False)
-    compare_bf16(run_tp(cuda_lib, tp, "bulk_ring"), oracle_tp(tp))
+    compare_bf16(run_tp(cuda_lib, tp, "bulk"), oracle_tp(tp))
 
 
 # ---------------------------------------------------------------------------
@@ -345,4 +346,4 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
     assert cuda_lib.device_status(clear=True) == 7
     assert cuda_lib.device_status(clear=True) == 0
     case = small_case(8, seed=30)
-    compare_bf16(run_tp(cuda_lib, case, "bulk_ring"), oracle_tp(case))
+    compare_bf16(run_tp(cuda_lib, case, "bulk"), oracle_tp(case))
