@@ -56,13 +56,17 @@ mf_status device_info(const DeviceInfo **out) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Finalize + RMSNorm: up to kClusterMaxTokens tokens the cluster kernel
-// spreads each token's gather over 8 SMs; above it one CTA per token.
-constexpr int64_t kClusterMaxTokens = 8;
+// Finalize + RMSNorm: below kBulkMinTokens tokens the register kernel has the
+// lowest latency (one dependent index load, then all row loads at once); from
+// there on the bulk-staged kernel keeps more bytes in flight per SM.  The
+// cluster kernel is never the fastest on a GB300 (cluster launch and two
+// cluster barriers cost more than spreading a token's 64 KB over 8 SMs saves)
+// and is only run when asked for.
+constexpr int64_t kBulkMinTokens = 1024;
 
 mf_variant pick_tp(int64_t num_tokens) {
     if (num_tokens <= 0) return MF_VARIANT_AUTO;
-    return num_tokens <= kClusterMaxTokens ? MF_VARIANT_CLUSTER : MF_VARIANT_TOKEN_CTA;
+    return num_tokens < kBulkMinTokens ? MF_VARIANT_TOKEN_CTA : MF_VARIANT_BULK;
 }
 
 // Beam: one CTA per live token with the token's block staged in shared memory.

@@ -140,7 +140,7 @@ def test_finalize_32768_tokens_full_size(cuda_lib, before):
     # the bandwidth workload in the launch configuration the benchmark times
     # (automatic choice), every output element against the oracle
     case = c_roofline()
-    assert cuda_lib.select_finalize_variant(case.num_tokens) == "token_cta"
+    assert cuda_lib.select_finalize_variant(case.num_tokens) == "bulk"
     got = run_tp(cuda_lib, case, "auto", before=before)
     stats = compare_bf16(got, oracle_tp(case, before=before))
     assert stats["n"] == 32768 * 4096
