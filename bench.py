@@ -63,11 +63,13 @@ def reduce_max(value: float, group=None) -> float:
     return float(t.item())
 
 
-def source_digest() -> str:
-    """Digest of the kernel sources; a recorded traffic figure applies only
-    to the sources it was measured on."""
+def source_digest(kernel: str) -> str:
+    """Digest of the sources a kernel is built from (its family's .cu file and
+    the shared device headers); a recorded traffic figure applies only to the
+    sources it was measured on."""
+    family = "beam_finalize.cu" if kernel.startswith("beam_") else "tp_finalize.cu"
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
+    for name in ("common.cuh", "kernels.h", family):
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
@@ -80,7 +82,7 @@ def recorded_traffic(kernel: str, workload: str) -> float | None:
     ``traffic: kernel=<name> workload=<name> bytes_per_launch=<n> sources=<digest>``"""
     if not os.path.isdir(PROFILES):
         return None
-    digest = source_digest()
+    digest = source_digest(kernel)
     pat = re.compile(r"traffic: kernel=(\S+) workload=(\S+) bytes_per_launch=(\d+) sources=(\S+)")
     for name in sorted(os.listdir(PROFILES)):
         if not name.endswith((".md", ".txt")):
@@ -399,18 +401,39 @@ def run_ours(args) -> None:
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(device)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        ev[i][0].record(stream)
-        job.launch(i)
-        ev[i][1].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize(device)
-    t_wall1 = time.time()
+    if args.graph:
+        # decode sizes: the K launches replay from one CUDA graph, so the timed
+        # region holds no host launch gaps (the per-launch figure is the mean)
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap), torch.cuda.graph(graph, stream=cap):
+            for i in range(args.steps):
+                job.launch(i)
+        torch.cuda.synchronize(device)
+        graph.replay()  # one untimed replay
+        torch.cuda.synchronize(device)
+        t_wall0 = time.time()
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        t_wall1 = time.time()
+        launch_ms = [start.elapsed_time(end) / args.steps] * args.steps
+    else:
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        t_wall0 = time.time()
+        start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            job.launch(i)
+            ev[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        t_wall1 = time.time()
+        launch_ms = [a.elapsed_time(b) for a, b in ev]
     if world > 1:
         dist.barrier()
     clocks.stop()
@@ -418,7 +441,6 @@ def run_ours(args) -> None:
         raise SystemExit("device wait timeout in the timed region")
 
     elapsed_ms = reduce_max(start.elapsed_time(end))
-    launch_ms = [a.elapsed_time(b) for a, b in ev]
     avg_launch_ms = statistics.fmean(launch_ms)
     units = job.units_per_step * args.steps * world
     value = units / (elapsed_ms / 1e3)
@@ -444,6 +466,8 @@ def run_ours(args) -> None:
                          f"({job.bytes_per_launch / 1e9:.3f} GB per launch, L2 is 0.13 GB)"
                    if job.bytes_per_launch > 256e6 else "inputs smaller than L2 (warm)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "timing": "one CUDA graph of all timed launches" if args.graph
+                   else "CUDA events around every launch",
                    **job.describe},
         "hbm_gbs": hbm_gbs,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -521,6 +545,8 @@ def parse_args(argv=None):
                    choices=("roofline", "padded", "beam", "small", "decode"))
     p.add_argument("--tokens", type=int, default=None, help="token count of --workload decode")
     p.add_argument("--variant", default="auto", choices=("auto", "token_cta", "bulk", "cluster"))
+    p.add_argument("--graph", action="store_true",
+                   help="replay the timed launches from one CUDA graph (decode sizes)")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")

@@ -56,16 +56,20 @@ mf_status device_info(const DeviceInfo **out) {
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Finalize + RMSNorm: below kBulkMinTokens tokens the register kernel has the
-// lowest latency (one dependent index load, then all row loads at once); from
-// there on the bulk-staged kernel keeps more bytes in flight per SM.  The
-// cluster kernel is never the fastest on a GB300 (cluster launch and two
-// cluster barriers cost more than spreading a token's 64 KB over 8 SMs saves)
-// and is only run when asked for.
+// Finalize + RMSNorm, by token count (measured on GB300):
+//   <= kClusterMaxTokens  cluster kernel: a token's gather spread over 8 SMs
+//                         (2.50 us per call at 1 token when the rows are in
+//                         L2, as right after the producing GEMM, against
+//                         2.61 us for one CTA per token);
+//   <  kBulkMinTokens     register kernel (one dependent index load, then all
+//                         row loads at once);
+//   otherwise             bulk-staged kernel (more bytes in flight per SM).
+constexpr int64_t kClusterMaxTokens = 8;
 constexpr int64_t kBulkMinTokens = 1024;
 
 mf_variant pick_tp(int64_t num_tokens) {
     if (num_tokens <= 0) return MF_VARIANT_AUTO;
+    if (num_tokens <= kClusterMaxTokens) return MF_VARIANT_CLUSTER;
     return num_tokens < kBulkMinTokens ? MF_VARIANT_TOKEN_CTA : MF_VARIANT_BULK;
 }
 

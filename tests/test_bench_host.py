@@ -64,7 +64,8 @@ def test_clock_summary_prefers_the_timed_window():
 
 def test_recorded_traffic_requires_matching_sources(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "PROFILES", str(tmp_path))
-    d = bench.source_digest()
+    d = bench.source_digest("tp_token_cta_kernel")
+    assert d != bench.source_digest("beam_token_bulk_kernel")
     (tmp_path / "k.md").write_text(
         f"traffic: kernel=tp_token_cta_kernel workload=w bytes_per_launch=123 sources={d}\n"
         "traffic: kernel=tp_token_cta_kernel workload=v bytes_per_launch=9 sources=stale\n")
