@@ -10,7 +10,8 @@ alternates between steps so both orderings are timed.  The inputs (2.42 GB
 per call) are larger than L2, so every call reads its rows from HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload roofline|padded|beam|small|decode] [--tokens T]
+                    [--workload roofline|padded|beam|small|decode|custom] [--tokens T]
+                    [--hidden H --top-k K --weights fp32|bf16|packed]
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle (the
 reference arm of this path) on the host cores instead.
@@ -210,7 +211,7 @@ def make_tp_job(torch, mf, case: si.TpCase, device, variant: str, alternate: boo
     nw = _dev_bf16(torch, case.norm_weight, device)
     out = torch.empty((case.num_tokens, case.hidden), dtype=torch.bfloat16, device=device)
     T = case.num_tokens
-    wbytes = 2 if case.weights.dtype == np.uint16 else 4
+    wbytes = case.weights.dtype.itemsize
 
     def launch(step: int, tensors=(g, w, idx, nw, out)):
         before = (step % 2 == 1) if alternate else case.weight_before_norm
@@ -218,9 +219,12 @@ def make_tp_job(torch, mf, case: si.TpCase, device, variant: str, alternate: boo
         mf.moe_finalize_rmsnorm(gg, ww, ii, nn, oo, eps=case.eps, gain_center=case.gain_center,
                                 weight_before_norm=before, variant=variant)
 
-    chosen = mf.select_finalize_variant(T) if variant == "auto" else variant
+    chosen = (mf.select_finalize_variant(T, case.hidden, case.top_k) if variant == "auto"
+              else variant)
     kernel = {"bulk": "tp_token_bulk_kernel", "token_cta": "tp_token_cta_kernel",
               "cluster": "tp_cluster_kernel"}[chosen]
+    if (case.hidden, case.top_k) != (4096, 8):
+        kernel = "tp_generic_bulk_kernel"
     job = Job(case.name, T, si.algorithmic_bytes_tp(T, case.hidden, case.top_k, wbytes), kernel,
               launch, case, {"variant": chosen})
     job.device_tensors = (g, w, idx, nw, out)
@@ -246,7 +250,8 @@ def make_beam_job(torch, mf, case: si.BeamCase, device, variant: str) -> Job:
     return job
 
 
-def workload_case(name: str, tokens: int | None, seed_rank: int):
+def workload_case(name: str, tokens: int | None, seed_rank: int, args_hidden: int = 4096,
+                  args_top_k: int = 8, args_weights: str = "fp32"):
     """Host inputs of a named workload (rank-dependent seed for N > 1)."""
     if name == "roofline":
         c = si.finalize_32768_tokens(False) if seed_rank == 0 else si.tp_case(
@@ -266,6 +271,13 @@ def workload_case(name: str, tokens: int | None, seed_rank: int):
     if name == "decode":
         T = tokens or 1
         return "tp", si.finalize_decode(T), f"finalize+RMSNorm decode num_tokens={T} rows={10 * T}"
+    if name == "custom":
+        T, H, K = tokens or 8192, args_hidden, args_top_k
+        c = si.tp_case(f"finalize_T{T}_H{H}_K{K}_{args_weights}", T, hidden=H, top_k=K,
+                       indexed_rows=T * K, invalid_frac=0.01, weights_dtype=args_weights,
+                       gain_center=1.0, eps=1e-6, seed=seed_rank)
+        return "tp", c, (f"finalize+RMSNorm num_tokens={T} hidden={H} top_k={K} "
+                         f"{args_weights} weights, 1% invalid, rows={T * K} ~N(0,1)")
     if name == "beam":
         return "beam", si.beam_8000_live(poison_dead_rows=False), (
             "Beam finalize capacity=8192 top_k=8 hidden=7168 live_tokens=8000 routed_scale=2.5 "
@@ -319,7 +331,8 @@ def run_reference(args) -> None:
         return
     import oracle
     oracle.build()
-    kind, case, desc = workload_case(args.workload, args.tokens, 0)
+    kind, case, desc = workload_case(args.workload, args.tokens, 0, args.hidden, args.top_k,
+                                     args.weights)
     threads = os.cpu_count() or 1
     T = total_tokens(kind, case)
     # size each step so the whole run stays within about a minute of wall time
@@ -381,7 +394,8 @@ def run_ours(args) -> None:
         dist.barrier()
     import moe_finalize_rmsnorm_gb300 as mf
 
-    kind, case, desc = workload_case(args.workload, args.tokens, rank_seed(0, rank) if rank else 0)
+    kind, case, desc = workload_case(args.workload, args.tokens, rank_seed(0, rank) if rank else 0,
+                                     args.hidden, args.top_k, args.weights)
     if kind == "tp":
         job = make_tp_job(torch, mf, case, device, args.variant,
                           alternate=args.workload == "roofline")
@@ -542,8 +556,13 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="roofline",
-                   choices=("roofline", "padded", "beam", "small", "decode"))
-    p.add_argument("--tokens", type=int, default=None, help="token count of --workload decode")
+                   choices=("roofline", "padded", "beam", "small", "decode", "custom"))
+    p.add_argument("--tokens", type=int, default=None,
+                   help="token count of --workload decode / custom")
+    p.add_argument("--hidden", type=int, default=4096, help="hidden size of --workload custom")
+    p.add_argument("--top-k", type=int, default=8, help="top-k of --workload custom")
+    p.add_argument("--weights", default="fp32", choices=("fp32", "bf16", "packed"),
+                   help="routing weight storage of --workload custom")
     p.add_argument("--variant", default="auto", choices=("auto", "token_cta", "bulk", "cluster"))
     p.add_argument("--graph", action="store_true",
                    help="replay the timed launches from one CUDA graph (decode sizes)")

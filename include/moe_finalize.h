@@ -60,9 +60,16 @@ typedef enum mf_status {
     MF_ERR_INVALID = 8           /* inconsistent argument combination or unknown variant */
 } mf_status;
 
+/* Storage of the routing weights.  MF_DTYPE_PACKED_TOPK takes the producer
+ * MoE's packed int32 routing words as they are: (expert_id << 16) |
+ * (bits of the BF16 weight), the topk_ids format of
+ * flashinfer.fused_moe.trtllm_fp8_per_tensor_scale_routed_moe (parameter
+ * list); the weight is the low 16 bits read as BF16, the expert id is ignored
+ * (the row comes from the index map). */
 typedef enum mf_dtype {
     MF_DTYPE_BF16 = 0,
-    MF_DTYPE_FP32 = 1
+    MF_DTYPE_FP32 = 1,
+    MF_DTYPE_PACKED_TOPK = 2
 } mf_dtype;
 
 /* Kernel choice.  AUTO picks by size; the others force one kernel (for
@@ -89,8 +96,9 @@ typedef enum mf_variant {
  *                    16-byte aligned (so every row start is).  May be NULL
  *                    only when rows == 0.
  *   rows             number of rows; an index i is valid iff 0 <= i < rows.
- *   expert_weights   device, [num_tokens, top_k] contiguous, BF16 or FP32
- *                    (weights_dtype); converted to FP32.  16-byte aligned.
+ *   expert_weights   device, [num_tokens, top_k] contiguous, BF16, FP32 or
+ *                    packed int32 routing words (weights_dtype); converted to
+ *                    FP32.  16-byte aligned.
  *   expanded_idx_to_permuted_idx
  *                    device, int32 [num_tokens, top_k] contiguous, 16-byte
  *                    aligned.  A negative or out-of-range index contributes
@@ -98,7 +106,10 @@ typedef enum mf_variant {
  *   norm_weight      device, BF16 [hidden], 16-byte aligned.
  *   output           device, BF16 [num_tokens, hidden] contiguous, 16-byte
  *                    aligned.
- *   hidden, top_k    must be 4096 and 8 (the operation is defined for these).
+ *   hidden, top_k    4096 and 8, the sizes the operation is defined for (the
+ *                    specialised kernels), or any hidden in 256..8192 that is
+ *                    a multiple of 256 with top_k in 1..32 (the range the Beam
+ *                    wrapper accepts; one generic kernel, variant AUTO or BULK).
  *   eps              added to the mean square inside the square root.
  *   gain_center      added to norm_weight in FP32: g = float(norm_weight) + gain_center.
  *   weight_before_norm  nonzero: y = v / rms(v) with v = acc * g;
@@ -110,7 +121,8 @@ typedef enum mf_variant {
  * rounded to nearest even.
  *
  * Errors: MF_ERR_SHAPE (num_tokens < 0, rows < 0, row_stride < hidden or not
- * a multiple of 8), MF_ERR_UNSUPPORTED (hidden != 4096 or top_k != 8),
+ * a multiple of 8), MF_ERR_UNSUPPORTED (hidden / top_k outside the sizes
+ * above), MF_ERR_INVALID (TOKEN_CTA or CLUSTER for sizes other than 4096 / 8),
  * MF_ERR_NULL, MF_ERR_ALIGN, MF_ERR_DTYPE, MF_ERR_CUDA.
  */
 mf_status moe_finalize_rmsnorm(const void *gemm2_permuted, int64_t rows, int64_t row_stride,
@@ -177,9 +189,10 @@ mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity
                                     float post_eps, int has_post_norm, mf_variant variant,
                                     mf_stream_t stream);
 
-/* The kernel AUTO would run for moe_finalize_rmsnorm with num_tokens tokens
- * on the current device (MF_VARIANT_AUTO if none would run). */
-mf_variant mf_select_finalize_variant(int64_t num_tokens);
+/* The kernel AUTO would run for moe_finalize_rmsnorm with these sizes
+ * (MF_VARIANT_AUTO if none would run: no tokens or unsupported sizes).  Sizes
+ * other than 4096 / 8 always run the generic bulk-staged kernel (MF_VARIANT_BULK). */
+mf_variant mf_select_finalize_variant(int64_t num_tokens, int32_t hidden, int32_t top_k);
 
 /* The kernel AUTO would run for beam_moe_finalize. */
 mf_variant mf_select_beam_variant(int64_t live_tokens, int32_t top_k, int32_t hidden);

@@ -17,7 +17,7 @@ import ctypes
 
 import torch
 
-from ._abi import (MF_DTYPE_BF16, MF_DTYPE_FP32, VARIANT_NAMES, VARIANTS, MoeFinalizeError,
+from ._abi import (MF_DTYPE_BF16, MF_DTYPE_FP32, MF_DTYPE_PACKED_TOPK, VARIANT_NAMES, VARIANTS, MoeFinalizeError,
                    check, lib)
 
 __all__ = [
@@ -50,12 +50,15 @@ def moe_finalize_rmsnorm(gemm2_permuted: torch.Tensor, expert_weights: torch.Ten
                          output: torch.Tensor, *, eps: float, gain_center: float,
                          weight_before_norm: bool, variant: str = "auto",
                          stream: torch.cuda.Stream | None = None) -> None:
-    """Finalize + RMSNorm into ``output`` (BF16 [num_tokens, 4096]).
+    """Finalize + RMSNorm into ``output`` (BF16 [num_tokens, hidden]).
 
     gemm2_permuted: BF16 (rows, >= 4096), unit last-dim stride, row stride a
-    multiple of 8.  expert_weights: BF16 or FP32 (num_tokens, 8).
-    expanded_idx_to_permuted_idx: int32 (num_tokens, 8); negative or
-    out-of-range entries contribute zero.  norm_weight: BF16 (4096,).
+    multiple of 8.  expert_weights: (num_tokens, top_k) BF16, FP32, or int32
+    packed routing words ``(expert_id << 16) | bf16 weight bits`` (the
+    producer MoE's topk_ids).  expanded_idx_to_permuted_idx: int32
+    (num_tokens, top_k); negative or out-of-range entries contribute zero.
+    norm_weight: BF16 (hidden,).  hidden 4096 with top_k 8, or hidden
+    256..8192 (a multiple of 256) with top_k 1..32.
     Asynchronous on ``stream`` (default: the current stream).
     """
     g, w, idx, nw, out = gemm2_permuted, expert_weights, expanded_idx_to_permuted_idx, \
@@ -66,8 +69,9 @@ def moe_finalize_rmsnorm(gemm2_permuted: torch.Tensor, expert_weights: torch.Ten
          "output must be a contiguous 2-D BF16 tensor")
     _req(idx.dim() == 2 and idx.dtype == torch.int32 and idx.is_contiguous(),
          "expanded_idx_to_permuted_idx must be a contiguous 2-D int32 tensor")
-    _req(w.dtype in (torch.bfloat16, torch.float32) and w.is_contiguous() and w.shape == idx.shape,
-         "expert_weights must be contiguous BF16 or FP32 with the index map's shape")
+    _req(w.dtype in (torch.bfloat16, torch.float32, torch.int32) and w.is_contiguous() and
+         w.shape == idx.shape,
+         "expert_weights must be contiguous BF16, FP32 or packed int32 with the index map's shape")
     _req(nw.dim() == 1 and nw.dtype == torch.bfloat16 and nw.is_contiguous(),
          "norm_weight must be a contiguous 1-D BF16 tensor")
     _req(out.shape[0] == idx.shape[0], "output and the index map disagree on num_tokens")
@@ -79,7 +83,8 @@ def moe_finalize_rmsnorm(gemm2_permuted: torch.Tensor, expert_weights: torch.Ten
     with torch.cuda.device(dev):
         st = lib().moe_finalize_rmsnorm_variant(
             g.data_ptr(), g.shape[0], row_stride, w.data_ptr(),
-            MF_DTYPE_BF16 if w.dtype == torch.bfloat16 else MF_DTYPE_FP32, idx.data_ptr(),
+            {torch.bfloat16: MF_DTYPE_BF16, torch.float32: MF_DTYPE_FP32,
+             torch.int32: MF_DTYPE_PACKED_TOPK}[w.dtype], idx.data_ptr(),
             nw.data_ptr(), out.data_ptr(), out.shape[0], out.shape[1], idx.shape[1], float(eps),
             float(gain_center), int(bool(weight_before_norm)), _variant(variant),
             _stream_ptr(stream, dev))
@@ -128,9 +133,10 @@ def beam_moe_finalize(expert_outputs: torch.Tensor, expert_weights: torch.Tensor
     return out
 
 
-def select_finalize_variant(num_tokens: int) -> str:
-    """Kernel the automatic choice runs for ``num_tokens`` (current device)."""
-    return VARIANT_NAMES[lib().mf_select_finalize_variant(int(num_tokens))]
+def select_finalize_variant(num_tokens: int, hidden: int = HIDDEN, top_k: int = TOP_K) -> str:
+    """Kernel the automatic choice runs for these sizes."""
+    return VARIANT_NAMES[lib().mf_select_finalize_variant(int(num_tokens), int(hidden),
+                                                          int(top_k))]
 
 
 def select_beam_variant(live_tokens: int, top_k: int, hidden: int) -> str:

@@ -15,7 +15,7 @@ STATUS_NAMES = {
     0: "MF_OK", 1: "MF_ERR_NULL", 2: "MF_ERR_SHAPE", 3: "MF_ERR_ALIGN", 4: "MF_ERR_DTYPE",
     5: "MF_ERR_UNSUPPORTED", 6: "MF_ERR_CUDA", 7: "MF_ERR_DEVICE_TIMEOUT", 8: "MF_ERR_INVALID",
 }
-MF_DTYPE_BF16, MF_DTYPE_FP32 = 0, 1
+MF_DTYPE_BF16, MF_DTYPE_FP32, MF_DTYPE_PACKED_TOPK = 0, 1, 2
 VARIANTS = {"auto": 0, "token_cta": 1, "bulk": 2, "cluster": 3}
 VARIANT_NAMES = {v: k for k, v in VARIANTS.items()}
 
@@ -29,7 +29,7 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_variant": (_int, _TP_ARGS + [_int, _vp]),
     "beam_moe_finalize": (_int, _BEAM_ARGS + [_vp]),
     "beam_moe_finalize_variant": (_int, _BEAM_ARGS + [_int, _vp]),
-    "mf_select_finalize_variant": (_int, [_i64]),
+    "mf_select_finalize_variant": (_int, [_i64, _i32, _i32]),
     "mf_select_beam_variant": (_int, [_i64, _i32, _i32]),
     "mf_status_string": (ctypes.c_char_p, [_int]),
     "mf_device_status": (_int, [_int]),

@@ -43,7 +43,7 @@ mf_status device_info(const DeviceInfo **out) {
                                    dev) != cudaSuccess ||
             cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status_word) !=
                 cudaSuccess ||
-            mf::prepare_tp_kernels(d.smem_optin) != cudaSuccess ||
+            mf::prepare_tp_kernels(d.smem_optin, d.smem_per_sm) != cudaSuccess ||
             mf::prepare_beam_kernels(d.smem_per_sm) != cudaSuccess) {
             (void)cudaGetLastError();
             return MF_ERR_CUDA;
@@ -108,10 +108,17 @@ mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
                                        float eps, float gain_center, int weight_before_norm,
                                        mf_variant variant, mf_stream_t stream) {
     if (num_tokens < 0 || rows < 0) return MF_ERR_SHAPE;
-    if (hidden != mf::kTpHidden || top_k != mf::kTpTopK) return MF_ERR_UNSUPPORTED;
+    const bool specialised = hidden == mf::kTpHidden && top_k == mf::kTpTopK;
+    if (!specialised && (hidden < 256 || hidden > 8192 || hidden % 256 != 0 || top_k < 1 ||
+                         top_k > 32))
+        return MF_ERR_UNSUPPORTED;
     if (row_stride < hidden || row_stride % 8 != 0) return MF_ERR_SHAPE;
-    if (weights_dtype != MF_DTYPE_BF16 && weights_dtype != MF_DTYPE_FP32) return MF_ERR_DTYPE;
+    if (weights_dtype != MF_DTYPE_BF16 && weights_dtype != MF_DTYPE_FP32 &&
+        weights_dtype != MF_DTYPE_PACKED_TOPK)
+        return MF_ERR_DTYPE;
     if (variant < MF_VARIANT_AUTO || variant > MF_VARIANT_CLUSTER) return MF_ERR_INVALID;
+    if (!specialised && variant != MF_VARIANT_AUTO && variant != MF_VARIANT_BULK)
+        return MF_ERR_INVALID;
     if (num_tokens == 0) return MF_OK;
     if (!expert_weights || !expanded_idx_to_permuted_idx || !norm_weight || !output ||
         (rows > 0 && !gemm2_permuted))
@@ -135,19 +142,24 @@ mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
     a.norm_weight = static_cast<const uint16_t *>(norm_weight);
     a.out = static_cast<uint16_t *>(output);
     a.num_tokens = num_tokens;
+    a.hidden = hidden;
+    a.top_k = top_k;
     a.eps = eps;
     a.gain_center = gain_center;
     a.before = weight_before_norm ? 1 : 0;
     a.status = d->status;
     a.timeout_ns = kWaitLimitNs;
-    const bool bf16w = weights_dtype == MF_DTYPE_BF16;
+    const int wk = weights_dtype == MF_DTYPE_BF16   ? mf::kWeightBF16
+                   : weights_dtype == MF_DTYPE_FP32 ? mf::kWeightFP32
+                                                    : mf::kWeightPacked;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
+    if (!specialised) return from_launch(mf::launch_tp_generic(a, wk, d->smem_per_sm, s));
     if (variant == MF_VARIANT_AUTO) variant = pick_tp(num_tokens);
     switch (variant) {
-        case MF_VARIANT_CLUSTER: return from_launch(mf::launch_tp_cluster(a, bf16w, s));
-        case MF_VARIANT_TOKEN_CTA: return from_launch(mf::launch_tp_token_cta(a, bf16w, s));
-        case MF_VARIANT_BULK: return from_launch(mf::launch_tp_bulk(a, bf16w, s));
+        case MF_VARIANT_CLUSTER: return from_launch(mf::launch_tp_cluster(a, wk, s));
+        case MF_VARIANT_TOKEN_CTA: return from_launch(mf::launch_tp_token_cta(a, wk, s));
+        case MF_VARIANT_BULK: return from_launch(mf::launch_tp_bulk(a, wk, s));
         default: return MF_ERR_INVALID;
     }
 }
@@ -219,7 +231,13 @@ mf_status beam_moe_finalize(const void *expert_outputs, int64_t capacity,
                                      post_eps, has_post_norm, MF_VARIANT_AUTO, stream);
 }
 
-mf_variant mf_select_finalize_variant(int64_t num_tokens) { return pick_tp(num_tokens); }
+mf_variant mf_select_finalize_variant(int64_t num_tokens, int32_t hidden, int32_t top_k) {
+    if (num_tokens <= 0) return MF_VARIANT_AUTO;
+    if (hidden == mf::kTpHidden && top_k == mf::kTpTopK) return pick_tp(num_tokens);
+    if (hidden < 256 || hidden > 8192 || hidden % 256 != 0 || top_k < 1 || top_k > 32)
+        return MF_VARIANT_AUTO;
+    return MF_VARIANT_BULK;
+}
 
 mf_variant mf_select_beam_variant(int64_t live_tokens, int32_t top_k, int32_t hidden) {
     (void)top_k;

@@ -12,15 +12,22 @@ constexpr int kTpHidden = 4096;
 constexpr int kTpTopK = 8;
 constexpr int kTpRowBytes = kTpHidden * 2;
 
+// How the routing weights are stored: BF16, FP32, or the producer's packed
+// int32 routing words (expert_id << 16) | bf16 weight bits, whose low half is
+// the weight.
+enum WeightKind : int { kWeightBF16 = 0, kWeightFP32 = 1, kWeightPacked = 2 };
+
 struct TpArgs {
     const uint16_t *gemm2;       // BF16 [rows, ld]
     int64_t rows;
     int64_t ld;                  // row stride in elements
-    const void *weights;         // [T, 8] BF16 or FP32
-    const int32_t *idx;          // [T, 8]
-    const uint16_t *norm_weight; // BF16 [4096]
-    uint16_t *out;               // BF16 [T, 4096]
+    const void *weights;         // [T, K] BF16, FP32 or packed int32
+    const int32_t *idx;          // [T, K]
+    const uint16_t *norm_weight; // BF16 [H]
+    uint16_t *out;               // BF16 [T, H]
     int64_t num_tokens;
+    int hidden;                  // H (4096 for the specialised kernels)
+    int top_k;                   // K (8 for the specialised kernels)
     float eps;
     float gain_center;
     int before;                  // weight_before_norm
@@ -46,12 +53,15 @@ struct BeamArgs {
 // Per-device one-time set-up (kernel attributes).  `smem_optin` is the
 // device's opt-in shared memory per block, `smem_per_sm` its shared memory
 // per multiprocessor.
-cudaError_t prepare_tp_kernels(int smem_optin);
+cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm);
 cudaError_t prepare_beam_kernels(int smem_per_sm);
 
-cudaError_t launch_tp_token_cta(const TpArgs &a, bool bf16_weights, cudaStream_t s);
-cudaError_t launch_tp_cluster(const TpArgs &a, bool bf16_weights, cudaStream_t s);
-cudaError_t launch_tp_bulk(const TpArgs &a, bool bf16_weights, cudaStream_t s);
+// Hidden 4096, top-k 8.
+cudaError_t launch_tp_token_cta(const TpArgs &a, int weight_kind, cudaStream_t s);
+cudaError_t launch_tp_cluster(const TpArgs &a, int weight_kind, cudaStream_t s);
+cudaError_t launch_tp_bulk(const TpArgs &a, int weight_kind, cudaStream_t s);
+// Any hidden in 256..8192 (multiple of 256) and top-k in 1..32.
+cudaError_t launch_tp_generic(const TpArgs &a, int weight_kind, int smem_per_sm, cudaStream_t s);
 
 cudaError_t launch_beam_token_cta(const BeamArgs &a, cudaStream_t s);
 cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, cudaStream_t s);

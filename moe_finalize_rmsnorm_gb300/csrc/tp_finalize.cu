@@ -1,4 +1,6 @@
-// Finalize + RMSNorm kernels for hidden 4096, top-k 8 (sm_103a).
+// Finalize + RMSNorm kernels (sm_103a): specialised kernels for hidden 4096,
+// top-k 8, and a generic kernel for hidden 256..8192 (multiple of 256) and
+// top-k 1..32.
 //
 // Operation (flashinfer.comm.tp_moe_finalize_rmsnorm, API page):
 //   acc[h] = sum over valid slots k (0 <= idx[t,k] < rows), ascending k,
@@ -25,6 +27,13 @@
 //                        (cp.async.bulk) completing on one mbarrier, so no
 //                        registers are held by data in flight and three
 //                        CTAs (192 KB of rows) fit per SM.
+//   tp_generic_bulk_kernel  any (hidden, top-k) in range: the staged design
+//                        with runtime sizes; the valid rows are copied in
+//                        pieces that fit half an SM's shared memory.
+//
+// Routing weights may be BF16, FP32 or the producer's packed int32 routing
+// words (expert_id << 16) | bf16 weight bits (trtllm_fp8_per_tensor_scale_
+// routed_moe, topk_ids parameter), whose low half is the weight.
 //
 // Every wait on an mbarrier is bounded (TpArgs::timeout_ns); a wait that gives
 // up ORs kStatusWaitTimeout into the device status word and the kernel returns.
@@ -39,17 +48,23 @@ constexpr int kChunksPerRow = kTpHidden / kChunkElems;  // 512
 
 // Load the 8 route entries of token t (same address across the block: the
 // loads are broadcasts).
-template <bool BF16W>
+template <int WK>
 __device__ __forceinline__ void load_route(const TpArgs &a, int64_t t, int (&idx)[8],
                                            float (&w)[8]) {
     const int4 *ip = reinterpret_cast<const int4 *>(a.idx + t * kTpTopK);
     const int4 i0 = __ldg(ip), i1 = __ldg(ip + 1);
     idx[0] = i0.x; idx[1] = i0.y; idx[2] = i0.z; idx[3] = i0.w;
     idx[4] = i1.x; idx[5] = i1.y; idx[6] = i1.z; idx[7] = i1.w;
-    if constexpr (BF16W) {
+    if constexpr (WK == kWeightBF16) {
         const uint4 q = __ldg(reinterpret_cast<const uint4 *>(
             static_cast<const uint16_t *>(a.weights) + t * kTpTopK));
         unpack8(q, w);
+    } else if constexpr (WK == kWeightPacked) {
+        const uint4 *pp = reinterpret_cast<const uint4 *>(
+            static_cast<const int32_t *>(a.weights) + t * kTpTopK);
+        const uint4 p0 = __ldg(pp), p1 = __ldg(pp + 1);
+        w[0] = bf16_lo(p0.x); w[1] = bf16_lo(p0.y); w[2] = bf16_lo(p0.z); w[3] = bf16_lo(p0.w);
+        w[4] = bf16_lo(p1.x); w[5] = bf16_lo(p1.y); w[6] = bf16_lo(p1.z); w[7] = bf16_lo(p1.w);
     } else {
         const float4 *wp = reinterpret_cast<const float4 *>(
             static_cast<const float *>(a.weights) + t * kTpTopK);
@@ -106,7 +121,7 @@ __device__ __forceinline__ void scale_store(const float (&acc)[CPT][8], const fl
 // ---------------------------------------------------------------------------
 // one CTA per token
 
-template <int CPT, bool BF16W>
+template <int CPT, int WK>
 __global__ void __launch_bounds__(kChunksPerRow / CPT)
     tp_token_cta_kernel(const TpArgs a) {
     constexpr int NT = kChunksPerRow / CPT;
@@ -118,7 +133,7 @@ __global__ void __launch_bounds__(kChunksPerRow / CPT)
 
     int idx[8];
     float w[8];
-    load_route<BF16W>(a, t, idx, w);
+    load_route<WK>(a, t, idx, w);
 
     // issue every gather before the first use
     uint4 q[8][CPT];
@@ -168,7 +183,7 @@ __global__ void __launch_bounds__(kChunksPerRow / CPT)
 // ---------------------------------------------------------------------------
 // decode sizes: a cluster of C CTAs per token
 
-template <int C, bool BF16W>
+template <int C, int WK>
 __global__ void __launch_bounds__(kChunksPerRow / C) tp_cluster_kernel(const TpArgs a) {
     constexpr int NT = kChunksPerRow / C;  // one chunk per thread
     constexpr int NW = NT / 32;
@@ -182,7 +197,7 @@ __global__ void __launch_bounds__(kChunksPerRow / C) tp_cluster_kernel(const TpA
 
     int idx[8];
     float w[8];
-    load_route<BF16W>(a, t, idx, w);
+    load_route<WK>(a, t, idx, w);
 
     uint4 q[8];
 #pragma unroll
@@ -240,7 +255,7 @@ constexpr int kBulkCPT = 2;                      // 256 threads
 constexpr int kBulkThreads = kChunksPerRow / kBulkCPT;
 constexpr int kBulkSmem = kTpTopK * kTpRowBytes;  // 64 KB of rows
 
-template <bool BF16W>
+template <int WK>
 __global__ void __launch_bounds__(kBulkThreads)
     tp_token_bulk_kernel(const TpArgs a) {
     constexpr int NT = kBulkThreads, NW = NT / 32, CPT = kBulkCPT;
@@ -255,7 +270,7 @@ __global__ void __launch_bounds__(kBulkThreads)
 
     int idx[8];
     float w[8];
-    load_route<BF16W>(a, t, idx, w);
+    load_route<WK>(a, t, idx, w);
     uint32_t mask = 0;
 #pragma unroll
     for (int k = 0; k < 8; ++k) mask |= (slot_valid(idx[k], a.rows) ? 1u : 0u) << k;
@@ -314,36 +329,186 @@ __global__ void __launch_bounds__(kBulkThreads)
     if (ok) scale_store<CPT, NT>(acc, g, before, r, a.out + t * kTpHidden, tid);
 }
 
+// ---------------------------------------------------------------------------
+// any hidden / top-k: one CTA per token, valid rows staged in pieces
+
+// Warp 0 reads the route (lane k holds slot k), compacts the valid slots in
+// ascending k into shared memory, and thread 0 copies up to `rows_per_piece`
+// valid rows at a time into the staging buffer with one bulk copy per row.
+// Each thread owns CPT 16-byte chunks of the H columns.  Same arithmetic as
+// the specialised kernels: FP32 FMA over valid slots in ascending k, then the
+// RMSNorm epilogue with the mean over the H columns.
+template <int WK>
+__device__ __forceinline__ float load_weight(const void *weights, int64_t i) {
+    if constexpr (WK == kWeightBF16) {
+        const uint32_t b = __ldg(static_cast<const unsigned short *>(weights) + i);
+        return __uint_as_float(b << 16);
+    } else if constexpr (WK == kWeightPacked) {
+        return bf16_lo(static_cast<uint32_t>(__ldg(static_cast<const int32_t *>(weights) + i)));
+    } else {
+        return __ldg(static_cast<const float *>(weights) + i);
+    }
+}
+
+// Launch bounds: up to 512 threads with two CTAs per SM for CPT 2; up to
+// 1024 threads (hidden 256 x odd) for CPT 1.
+template <int CPT>
+constexpr int generic_max_threads() { return CPT == 2 ? 512 : 1024; }
+template <int CPT>
+constexpr int generic_min_blocks() { return CPT == 2 ? 2 : 1; }
+
+template <int CPT, int WK>
+__global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks<CPT>())
+    tp_generic_bulk_kernel(const TpArgs a, const int rows_per_piece) {
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    __shared__ uint64_t bar;
+    __shared__ float red[32];
+    __shared__ float w_s[32];
+    __shared__ int idx_s[32];
+    __shared__ int order_s[32];
+    __shared__ int nvalid_s;
+
+    const int NT = blockDim.x;
+    const int tid = threadIdx.x;
+    const int64_t t = blockIdx.x;
+    const int H = a.hidden, K = a.top_k;
+    const uint32_t row_bytes = static_cast<uint32_t>(H) * 2;
+    const uint32_t base = smem_u32(rows_smem);
+    const uint32_t bar_addr = smem_u32(&bar);
+
+    if (tid < 32) {
+        int i = -1;
+        float w = 0.f;
+        if (tid < K) i = __ldg(a.idx + t * K + tid);
+        const bool valid = tid < K && slot_valid(i, a.rows);
+        if (valid) w = load_weight<WK>(a.weights, t * K + tid);  // invalid slots: never read
+        const unsigned mask = __ballot_sync(0xffffffffu, valid);
+        idx_s[tid] = i;
+        w_s[tid] = w;
+        if (valid) order_s[__popc(mask & ((1u << tid) - 1u))] = tid;
+        if (tid == 0) {
+            nvalid_s = __popc(mask);
+            mbar_init(bar_addr, 1);
+            fence_mbar_init();
+        }
+    }
+    float g[CPT][8];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) load_gain(a, tid + c * NT, g[c]);
+    __syncthreads();
+
+    const int nvalid = nvalid_s;
+    float acc[CPT][8];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[c][j] = 0.f;
+
+    bool ok = true;
+    uint32_t phase = 0;
+    for (int p0 = 0; p0 < nvalid; p0 += rows_per_piece, phase ^= 1u) {
+        const int n = nvalid - p0 < rows_per_piece ? nvalid - p0 : rows_per_piece;
+        if (tid == 0) {
+            if (p0 > 0) fence_proxy_async_smem();  // earlier reads of the buffer come first
+            const uint64_t policy = policy_evict_first();
+            mbar_arrive_expect_tx(bar_addr, n * row_bytes);
+            for (int r = 0; r < n; ++r)
+                bulk_copy_g2s_hint(base + r * row_bytes,
+                                   a.gemm2 + static_cast<int64_t>(idx_s[order_s[p0 + r]]) * a.ld,
+                                   row_bytes, bar_addr, policy);
+        }
+        if (!mbar_wait(bar_addr, phase, a.timeout_ns)) {
+            atomicOr(a.status, kStatusWaitTimeout);
+            ok = false;
+            (void)mbar_wait(bar_addr, phase, a.timeout_ns);  // let copies in flight land
+        }
+        for (int r = 0; r < n; ++r) {
+            const float w = w_s[order_s[p0 + r]];
+            const uint32_t row = base + r * row_bytes;
+            uint4 q[CPT];
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) q[c] = lds_16(row + (tid + c * NT) * kChunkBytes);
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) {
+                float x[8];
+                unpack8(q[c], x);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[c][j] = __fmaf_rn(w, x[j], acc[c][j]);
+            }
+        }
+        if (p0 + rows_per_piece < nvalid) __syncthreads();  // the next piece reuses the buffer
+    }
+
+    const bool before = a.before != 0;
+    const float ss = warp_sum(prenorm<CPT>(acc, g, before));
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    const int nw = NT >> 5;
+    for (int i = 0; i < nw; ++i) tot += red[i];
+    const float r = rsqrtf(__fadd_rn(__fdiv_rn(tot, static_cast<float>(H)), a.eps));
+    if (!ok) return;
+    uint16_t *out_row = a.out + t * H;
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+        float y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float s = __fmul_rn(acc[c][j], r);
+            y[j] = before ? s : __fmul_rn(s, g[c][j]);
+        }
+        st_cs_16(out_row + static_cast<int64_t>(tid + c * NT) * kChunkElems, pack8_rn(y));
+    }
+}
+
+// 2 chunks per thread when that leaves at least 256 threads, else 1.
+int generic_cpt(int hidden) { return ((hidden / 256) % 2 == 0 && hidden / 16 >= 256) ? 2 : 1; }
+
+// Shared memory for one CTA's rows, sized so that two CTAs fit an SM (1 KB
+// system reservation and the static shared memory per CTA included).
+int generic_budget(int smem_per_sm) { return smem_per_sm / 2 - 1024 - 768; }
+
+int generic_rows(int smem_per_sm, int top_k, int hidden) {
+    const int rows = generic_budget(smem_per_sm) / (hidden * 2);
+    return rows < 1 ? 1 : (rows > top_k ? top_k : rows);
+}
+
+template <typename Kern>
+cudaError_t set_dyn_smem(Kern k, int bytes) {
+    return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
 }  // namespace
 
-cudaError_t prepare_tp_kernels(int smem_optin) {
+cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm) {
     (void)smem_optin;
-    cudaError_t e = cudaFuncSetAttribute(tp_token_bulk_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tp_token_bulk_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kBulkSmem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tp_cluster_kernel<16, false>,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tp_cluster_kernel<16, true>,
-                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    const int budget = generic_budget(smem_per_sm);
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightBF16>, kBulkSmem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightFP32>, kBulkSmem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightPacked>, kBulkSmem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightBF16>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightFP32>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightPacked>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightBF16>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightFP32>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightPacked>, budget);
     return e;
 }
 
-cudaError_t launch_tp_token_cta(const TpArgs &a, bool bf16_weights, cudaStream_t s) {
+cudaError_t launch_tp_token_cta(const TpArgs &a, int wk, cudaStream_t s) {
     constexpr int CPT = 1;
     const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(kChunksPerRow / CPT);
-    if (bf16_weights)
-        tp_token_cta_kernel<CPT, true><<<grid, block, 0, s>>>(a);
-    else
-        tp_token_cta_kernel<CPT, false><<<grid, block, 0, s>>>(a);
+    switch (wk) {
+        case kWeightBF16: tp_token_cta_kernel<CPT, kWeightBF16><<<grid, block, 0, s>>>(a); break;
+        case kWeightPacked: tp_token_cta_kernel<CPT, kWeightPacked><<<grid, block, 0, s>>>(a); break;
+        default: tp_token_cta_kernel<CPT, kWeightFP32><<<grid, block, 0, s>>>(a); break;
+    }
     return cudaGetLastError();
 }
 
 template <int C>
-static cudaError_t launch_cluster_c(const TpArgs &a, bool bf16_weights, cudaStream_t s) {
+static cudaError_t launch_cluster_c(const TpArgs &a, int wk, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.num_tokens * C));
     cfg.blockDim = dim3(kChunksPerRow / C);
@@ -356,20 +521,44 @@ static cudaError_t launch_cluster_c(const TpArgs &a, bool bf16_weights, cudaStre
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (bf16_weights) return cudaLaunchKernelEx(&cfg, tp_cluster_kernel<C, true>, a);
-    return cudaLaunchKernelEx(&cfg, tp_cluster_kernel<C, false>, a);
+    switch (wk) {
+        case kWeightBF16: return cudaLaunchKernelEx(&cfg, tp_cluster_kernel<C, kWeightBF16>, a);
+        case kWeightPacked: return cudaLaunchKernelEx(&cfg, tp_cluster_kernel<C, kWeightPacked>, a);
+        default: return cudaLaunchKernelEx(&cfg, tp_cluster_kernel<C, kWeightFP32>, a);
+    }
 }
 
-cudaError_t launch_tp_cluster(const TpArgs &a, bool bf16_weights, cudaStream_t s) {
-    return launch_cluster_c<8>(a, bf16_weights, s);
+cudaError_t launch_tp_cluster(const TpArgs &a, int wk, cudaStream_t s) {
+    return launch_cluster_c<8>(a, wk, s);
 }
 
-cudaError_t launch_tp_bulk(const TpArgs &a, bool bf16_weights, cudaStream_t s) {
+cudaError_t launch_tp_bulk(const TpArgs &a, int wk, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(kBulkThreads);
-    if (bf16_weights)
-        tp_token_bulk_kernel<true><<<grid, block, kBulkSmem, s>>>(a);
+    switch (wk) {
+        case kWeightBF16: tp_token_bulk_kernel<kWeightBF16><<<grid, block, kBulkSmem, s>>>(a); break;
+        case kWeightPacked: tp_token_bulk_kernel<kWeightPacked><<<grid, block, kBulkSmem, s>>>(a); break;
+        default: tp_token_bulk_kernel<kWeightFP32><<<grid, block, kBulkSmem, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+template <int CPT>
+static void launch_generic_cpt(const TpArgs &a, int wk, int rows, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(a.hidden / 8 / CPT);
+    const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;
+    switch (wk) {
+        case kWeightBF16: tp_generic_bulk_kernel<CPT, kWeightBF16><<<grid, block, bytes, s>>>(a, rows); break;
+        case kWeightPacked: tp_generic_bulk_kernel<CPT, kWeightPacked><<<grid, block, bytes, s>>>(a, rows); break;
+        default: tp_generic_bulk_kernel<CPT, kWeightFP32><<<grid, block, bytes, s>>>(a, rows); break;
+    }
+}
+
+cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, cudaStream_t s) {
+    const int rows = generic_rows(smem_per_sm, a.top_k, a.hidden);
+    if (generic_cpt(a.hidden) == 2)
+        launch_generic_cpt<2>(a, wk, rows, s);
     else
-        tp_token_bulk_kernel<false><<<grid, block, kBulkSmem, s>>>(a);
+        launch_generic_cpt<1>(a, wk, rows, s);
     return cudaGetLastError();
 }
 

@@ -93,13 +93,14 @@ def moe_finalize_rmsnorm(gemm2: np.ndarray, weights: np.ndarray, idx: np.ndarray
     """Oracle of tp_moe_finalize_rmsnorm.
 
     gemm2: uint16 [rows, row_stride] (BF16 bits; the first ``hidden`` columns
-    are live, default all).  weights: float32 or uint16 (BF16 bits)
-    [T, top_k].  idx: int32 [T, top_k].  norm_weight: uint16 [hidden].
+    are live, default all).  weights [T, top_k]: float32, uint16 (BF16 bits),
+    or int32 packed routing words ``(expert_id << 16) | bf16 bits`` (the
+    topk_ids format of trtllm_fp8_per_tensor_scale_routed_moe).  idx: int32 [T, top_k].  norm_weight: uint16 [hidden].
     Returns uint16 [T, hidden].
     """
     assert gemm2.dtype == np.uint16 and gemm2.ndim == 2
     assert idx.dtype == np.int32 and idx.ndim == 2 and weights.shape == idx.shape
-    assert weights.dtype in (np.float32, np.uint16)
+    assert weights.dtype in (np.float32, np.uint16, np.int32)
     rows, row_stride = gemm2.shape
     hidden = row_stride if hidden is None else int(hidden)
     assert 0 < hidden <= row_stride and norm_weight.shape == (hidden,)
@@ -108,7 +109,8 @@ def moe_finalize_rmsnorm(gemm2: np.ndarray, weights: np.ndarray, idx: np.ndarray
         out = np.empty((t, hidden), dtype=np.uint16)
     assert out.shape == (t, hidden) and out.dtype == np.uint16
     rc = _load().oracle_moe_finalize_rmsnorm(
-        _ptr(gemm2), rows, row_stride, _ptr(weights), int(weights.dtype == np.float32),
+        _ptr(gemm2), rows, row_stride, _ptr(weights),
+        {np.dtype(np.uint16): 0, np.dtype(np.float32): 1, np.dtype(np.int32): 2}[weights.dtype],
         _ptr(idx), _ptr(norm_weight), _ptr(out), t, hidden, k, float(eps),
         float(gain_center), int(bool(weight_before_norm)))
     if rc != 0:

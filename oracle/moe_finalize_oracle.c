@@ -128,14 +128,18 @@ static double inverse_rms(const double *v, int32_t hidden, double eps)
  *
  * gemm2:        BF16 bits, `rows` rows of `row_stride` elements; columns
  *               [0, hidden) are used.
- * weights:      [num_tokens, top_k], BF16 bits (weights_fp32 == 0) or float.
+ * weights:      [num_tokens, top_k]: BF16 bits (weights_kind 0), float
+ *               (weights_kind 1), or the producer MoE's packed int32 routing
+ *               words (weights_kind 2): (expert_id << 16) | BF16 weight bits,
+ *               the topk_ids format of trtllm_fp8_per_tensor_scale_routed_moe
+ *               (parameter list); the weight is the low half.
  * idx:          [num_tokens, top_k] int32.
  * norm_weight:  BF16 bits [hidden].
  * output:       BF16 bits [num_tokens, hidden].
  * Returns 0, or -1 if the scratch row could not be allocated.
  */
 int oracle_moe_finalize_rmsnorm(const uint16_t *gemm2, int64_t rows, int64_t row_stride,
-                                const void *weights, int weights_fp32, const int32_t *idx,
+                                const void *weights, int weights_kind, const int32_t *idx,
                                 const uint16_t *norm_weight, uint16_t *output,
                                 int64_t num_tokens, int32_t hidden, int32_t top_k,
                                 float eps, float gain_center, int weight_before_norm)
@@ -154,8 +158,14 @@ int oracle_moe_finalize_rmsnorm(const uint16_t *gemm2, int64_t rows, int64_t row
             int64_t i = idx[t * top_k + k];
             if (i < 0 || i >= rows)
                 continue; /* invalid slot: contributes nothing */
-            float w = weights_fp32 ? ((const float *)weights)[t * top_k + k]
-                                   : bf16_bits_to_float(((const uint16_t *)weights)[t * top_k + k]);
+            float w;
+            if (weights_kind == 1)
+                w = ((const float *)weights)[t * top_k + k];
+            else if (weights_kind == 2)
+                w = bf16_bits_to_float(
+                    (uint16_t)(((const uint32_t *)weights)[t * top_k + k] & 0xFFFFu));
+            else
+                w = bf16_bits_to_float(((const uint16_t *)weights)[t * top_k + k]);
             accumulate_row(acc, gemm2 + i * row_stride, w, hidden);
         }
         for (int32_t h = 0; h < hidden; ++h) {

@@ -29,7 +29,7 @@ import numpy as np
 BF16_NAN = np.uint16(0x7FC0)
 
 # tensor ids for SeedSequence([seed, id])
-_ID_ROWS, _ID_IDX, _ID_INVALID, _ID_LOGITS, _ID_NORM = 1, 2, 3, 4, 5
+_ID_ROWS, _ID_IDX, _ID_INVALID, _ID_LOGITS, _ID_NORM, _ID_EXPERT = 1, 2, 3, 4, 5, 6
 
 _CHUNK = 1 << 24  # elements per independently seeded chunk
 
@@ -79,6 +79,15 @@ def softmax_weights(tokens: int, top_k: int, seed: int, dtype: str) -> np.ndarra
     return _f32_to_bf16_bits(p)
 
 
+def pack_topk(weights_bf16: np.ndarray, seed: int, num_experts: int = 256) -> np.ndarray:
+    """int32 routing words ``(expert_id << 16) | bf16 bits`` (the producer MoE's
+    packed topk_ids layout) holding the given BF16 weights and random expert
+    ids in [0, num_experts)."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, _ID_EXPERT])))
+    experts = g.integers(0, num_experts, size=weights_bf16.shape).astype(np.uint32)
+    return ((experts << 16) | weights_bf16.astype(np.uint32)).view(np.int32)
+
+
 def permutation_index(tokens: int, top_k: int, indexed_rows: int, total_rows: int,
                       invalid_frac: float, seed: int) -> np.ndarray:
     """int32 [tokens, top_k]: a random injective map into rows [0, indexed_rows),
@@ -102,7 +111,7 @@ class TpCase:
     """Inputs of one tp_moe_finalize_rmsnorm call (host arrays)."""
     name: str
     gemm2: np.ndarray          # uint16 [rows, row_stride]
-    weights: np.ndarray        # float32 or uint16 [T, K]
+    weights: np.ndarray        # float32, uint16 (BF16) or int32 (packed) [T, K]
     idx: np.ndarray            # int32 [T, K]
     norm_weight: np.ndarray    # uint16 [hidden]
     hidden: int
@@ -155,7 +164,10 @@ def tp_case(name: str, tokens: int, *, hidden: int = 4096, top_k: int = 8,
         gemm2[:indexed_rows, :hidden] = live
         del live
     idx = permutation_index(tokens, top_k, indexed_rows, rows, invalid_frac, seed)
-    weights = softmax_weights(tokens, top_k, seed, weights_dtype)
+    if weights_dtype == "packed":
+        weights = pack_topk(softmax_weights(tokens, top_k, seed, "bf16"), seed)
+    else:
+        weights = softmax_weights(tokens, top_k, seed, weights_dtype)
     norm_weight = normal_bf16((hidden,), norm_sigma, seed, _ID_NORM, mu=norm_mu)
     return TpCase(name, gemm2, weights, idx, norm_weight, hidden, eps, gain_center,
                   weight_before_norm, meta=dict(indexed_rows=indexed_rows, rows=rows,

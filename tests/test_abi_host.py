@@ -64,13 +64,20 @@ def tp(lib, gemm2=A, rows=100, stride=4096, w=A, wdt=1, idx=A, nw=A, out=A, T=4,
 
 
 def test_tp_validation(lib):
-    assert tp(lib, H=7168) == UNSUP
-    assert tp(lib, K=4) == UNSUP
+    # sizes: 4096 / 8 (specialised) or hidden 256..8192 step 256, top_k 1..32
+    assert tp(lib, H=128) == UNSUP
+    assert tp(lib, H=8448) == UNSUP
+    assert tp(lib, H=4000) == UNSUP
+    assert tp(lib, K=0) == UNSUP
+    assert tp(lib, K=33) == UNSUP
+    assert tp(lib, K=4, variant=1) == INVALID     # register kernel only for 4096 / 8
+    assert tp(lib, H=2048, variant=3) == INVALID  # cluster kernel only for 4096 / 8
+    assert tp(lib, H=2048, stride=2044) == SHAPE
     assert tp(lib, stride=4095) == SHAPE          # shorter than hidden
     assert tp(lib, stride=4100) == SHAPE          # not a multiple of 8
     assert tp(lib, T=-1) == SHAPE
     assert tp(lib, rows=-1) == SHAPE
-    assert tp(lib, wdt=2) == DTYPE
+    assert tp(lib, wdt=3) == DTYPE
     assert tp(lib, variant=9) == INVALID
     assert tp(lib, gemm2=None) == NULL
     assert tp(lib, w=None) == NULL

@@ -126,6 +126,34 @@ def test_negative_weight_and_values_sign():
     assert vals(out[0]) == [0.6328125, 1.265625]
 
 
+def test_hand_example_packed_routing_words():
+    # the producer's packed words (expert_id << 16) | bf16 bits: expert 5 with
+    # 0.5 (0x3F00), expert 40000 with 0.25 (0x3E80; the word is negative as
+    # int32), and an invalid slot whose word holds a BF16 NaN -- the same sums
+    # as the unit-gain hand example, so the same output
+    gemm2, idx, _ = _p1_inputs()
+    packed = np.array([[(5 << 16) | 0x3F00, (40000 << 16) | 0x3E80, (0xFFFF << 16) | 0x7FC0]],
+                      dtype=np.uint32).view(np.int32)
+    out = oracle.moe_finalize_rmsnorm(gemm2, packed, idx, bits([1, 1, 1, 1]), eps=0.0,
+                                      gain_center=0.0, weight_before_norm=False)
+    assert vals(out[0]) == [0.79296875, 0.921875, 1.0546875, 1.1875]
+
+
+def test_packed_words_equal_bf16_weights():
+    # the expert id in the high half never matters; the low half is the weight
+    rng = np.random.default_rng(14)
+    gemm2, idx, w, nw = _random_case(rng)
+    wb = f32_to_bf16_bits(w)
+    experts = rng.integers(0, 65536, size=w.shape).astype(np.uint32)
+    packed = ((experts << 16) | wb.astype(np.uint32)).view(np.int32)
+    for before in (False, True):
+        a = oracle.moe_finalize_rmsnorm(gemm2, wb, idx, nw, eps=1e-6, gain_center=1.0,
+                                        weight_before_norm=before)
+        b = oracle.moe_finalize_rmsnorm(gemm2, packed, idx, nw, eps=1e-6, gain_center=1.0,
+                                        weight_before_norm=before)
+        assert np.array_equal(a, b)
+
+
 # --------------------------------------------------------------------------
 # closed forms
 

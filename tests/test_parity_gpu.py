@@ -269,13 +269,49 @@ def test_non_default_stream(cuda_lib):
     compare_bf16(got, oracle_tp(case))
 
 
+# ---------------------------------------------------------------------------
+# other sizes (hidden 256..8192, top_k 1..32) and packed routing words
+
+@pytest.mark.parametrize("H,K", [(256, 1), (256, 32), (7168, 8), (8192, 32), (4096, 4),
+                                 (2048, 16), (7936, 3), (1536, 5), (4096, 8)])
+@pytest.mark.parametrize("wdt", ["fp32", "bf16", "packed"])
+def test_generic_sizes(cuda_lib, H, K, wdt):
+    T = 37
+    case = si.tp_case(f"generic_{H}_{K}", T, hidden=H, top_k=K, indexed_rows=T * K + 5,
+                      padding_rows=3, row_stride=H + 16, invalid_frac=0.1, weights_dtype=wdt,
+                      seed=H + K, weight_before_norm=bool(K % 2), poison_padding=True)
+    case.idx[0, :] = -1                                  # one token with no valid slot
+    variants = ("auto", "bulk") if (H, K) != (4096, 8) else TP_VARIANTS
+    for v in variants:
+        compare_bf16(run_tp(cuda_lib, case, v), oracle_tp(case))
+
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_packed_routing_words_specialised(cuda_lib, variant):
+    case = si.tp_case("packed", 300, indexed_rows=2500, invalid_frac=0.03, weights_dtype="packed",
+                      seed=31)
+    assert case.weights.dtype == np.int32 and (case.weights < 0).sum() == 0
+    compare_bf16(run_tp(cuda_lib, case, variant), oracle_tp(case))
+    # high expert ids (negative words) change nothing
+    case.weights = (case.weights.view(np.uint32) | np.uint32(0xF0000000)).view(np.int32)
+    compare_bf16(run_tp(cuda_lib, case, variant), oracle_tp(case))
+
+
+def test_other_sizes_reject_register_and_cluster_kernels(cuda_lib):
+    case = si.tp_case("generic_reject", 4, hidden=2048, top_k=8, seed=32)
+    for v in ("token_cta", "cluster"):
+        with pytest.raises(cuda_lib.MoeFinalizeError) as e:
+            run_tp(cuda_lib, case, v)
+        assert e.value.status == 8
+
+
 def test_unsupported_hidden_raises(cuda_lib):
-    g = torch.zeros(16, 2048, dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros(16, 2000, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(cuda_lib.MoeFinalizeError) as e:
         cuda_lib.moe_finalize_rmsnorm(g, torch.zeros(2, 8, device="cuda"),
                                       torch.zeros(2, 8, dtype=torch.int32, device="cuda"),
-                                      torch.zeros(2048, dtype=torch.bfloat16, device="cuda"),
-                                      torch.zeros(2, 2048, dtype=torch.bfloat16, device="cuda"),
+                                      torch.zeros(2000, dtype=torch.bfloat16, device="cuda"),
+                                      torch.zeros(2, 2000, dtype=torch.bfloat16, device="cuda"),
                                       eps=1e-6, gain_center=1.0, weight_before_norm=False)
     assert e.value.status == 5
 
