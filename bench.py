@@ -393,6 +393,7 @@ def run_ours(args) -> None:
     if world > 1:
         dist.barrier()
     import moe_finalize_rmsnorm_gb300 as mf
+    mf.set_programmatic_launch(not args.no_pdl)
 
     kind, case, desc = workload_case(args.workload, args.tokens, rank_seed(0, rank) if rank else 0,
                                      args.hidden, args.top_k, args.weights)
@@ -482,6 +483,7 @@ def run_ours(args) -> None:
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "timing": "one CUDA graph of all timed launches" if args.graph
                    else "CUDA events around every launch",
+                   "programmatic_dependent_launch": not args.no_pdl,
                    **job.describe},
         "hbm_gbs": hbm_gbs,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -566,6 +568,8 @@ def parse_args(argv=None):
     p.add_argument("--variant", default="auto", choices=("auto", "token_cta", "bulk", "cluster"))
     p.add_argument("--graph", action="store_true",
                    help="replay the timed launches from one CUDA graph (decode sizes)")
+    p.add_argument("--no-pdl", action="store_true",
+                   help="launch without programmatic dependent launch")
     p.add_argument("--e2e-steps", type=int, default=5)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")

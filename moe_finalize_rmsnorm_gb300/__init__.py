@@ -23,7 +23,7 @@ from ._abi import (MF_DTYPE_BF16, MF_DTYPE_FP32, MF_DTYPE_PACKED_TOPK, VARIANT_N
 __all__ = [
     "moe_finalize_rmsnorm", "tp_moe_finalize_rmsnorm", "beam_moe_finalize", "MoeFinalizeError",
     "device_status", "selftest_wait_timeout", "select_finalize_variant", "select_beam_variant",
-    "version", "HIDDEN", "TOP_K",
+    "version", "set_programmatic_launch", "programmatic_launch", "HIDDEN", "TOP_K",
 ]
 
 HIDDEN = 4096
@@ -155,6 +155,15 @@ def selftest_wait_timeout(timeout_ns: int = 10_000_000,
     dev = torch.device("cuda", torch.cuda.current_device())
     check(lib().mf_selftest_wait_timeout(int(timeout_ns), _stream_ptr(stream, dev)),
           "mf_selftest_wait_timeout")
+
+
+def set_programmatic_launch(enable: bool) -> None:
+    """Turn programmatic dependent launch on or off for later calls (default on)."""
+    lib().mf_set_programmatic_launch(int(bool(enable)))
+
+
+def programmatic_launch() -> bool:
+    return bool(lib().mf_get_programmatic_launch())
 
 
 def version() -> int:

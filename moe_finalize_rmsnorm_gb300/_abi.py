@@ -35,6 +35,8 @@ SIGNATURES = {
     "mf_device_status": (_int, [_int]),
     "mf_selftest_wait_timeout": (_int, [_u64, _vp]),
     "mf_version": (_i32, []),
+    "mf_set_programmatic_launch": (None, [_int]),
+    "mf_get_programmatic_launch": (_int, []),
 }
 
 _lock = threading.Lock()

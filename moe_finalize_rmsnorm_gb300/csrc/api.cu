@@ -2,6 +2,7 @@
 // device status word.  Declarations and the contract are in
 // include/moe_finalize.h.
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/moe_finalize.h"
@@ -27,6 +28,7 @@ struct DeviceInfo {
 
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
+std::atomic<int> g_programmatic{1};  // programmatic dependent launch, on by default
 
 // Per-device set-up on first use: SM count, opt-in shared memory, the status
 // word's device address and the kernels' attributes.
@@ -99,6 +101,10 @@ const char *mf_status_string(mf_status s) {
 
 int32_t mf_version(void) { return 100; }
 
+void mf_set_programmatic_launch(int enable) { g_programmatic.store(enable ? 1 : 0); }
+
+int mf_get_programmatic_launch(void) { return g_programmatic.load(); }
+
 mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
                                        int64_t row_stride, const void *expert_weights,
                                        mf_dtype weights_dtype,
@@ -149,6 +155,7 @@ mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
     a.before = weight_before_norm ? 1 : 0;
     a.status = d->status;
     a.timeout_ns = kWaitLimitNs;
+    a.programmatic = g_programmatic.load() != 0;
     const int wk = weights_dtype == MF_DTYPE_BF16   ? mf::kWeightBF16
                    : weights_dtype == MF_DTYPE_FP32 ? mf::kWeightFP32
                                                     : mf::kWeightPacked;
@@ -214,6 +221,7 @@ mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity
     a.has_norm = has_post_norm ? 1 : 0;
     a.status = d->status;
     a.timeout_ns = kWaitLimitNs;
+    a.programmatic = g_programmatic.load() != 0;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     if (variant == MF_VARIANT_AUTO) variant = pick_beam(live_tokens);

@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
     const int K = a.top_k, H = a.hidden;
     const uint16_t *xt = a.x + t * K * static_cast<int64_t>(H);
     const float *wt = a.weights + t * K;
+    pdl_wait();
 
     float acc[CPT][8];
 #pragma unroll
@@ -141,6 +142,7 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
         rs = inv_rms(tot, H, a.post_eps);
     }
     beam_store<CPT>(acc, a, norm, rs, a.out + t * H, tid, NT);
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
         mbar_init(bar_addr, 1);
         fence_mbar_init();
     }
+    pdl_wait();
     if (tid < K) wsm[tid] = __ldg(a.weights + t * K + tid);
     __syncthreads();
 
@@ -226,6 +229,7 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
         rs = inv_rms(tot, H, a.post_eps);
     }
     if (ok) beam_store<CPT>(acc, a, norm, rs, a.out + t * H, tid, NT);
+    pdl_trigger();
 }
 
 // Chunks per thread of the register kernel: the largest of 4, 2, 1 that
@@ -280,12 +284,12 @@ cudaError_t prepare_beam_kernels(int smem_per_sm) {
 cudaError_t launch_beam_token_cta(const BeamArgs &a, cudaStream_t s) {
     const int cpt = beam_cpt(a.hidden);
     const dim3 grid(static_cast<unsigned>(a.live)), block(a.hidden / 8 / cpt);
+    const bool p = a.programmatic;
     switch (cpt) {
-        case 4: beam_token_cta_kernel<4><<<grid, block, 0, s>>>(a); break;
-        case 2: beam_token_cta_kernel<2><<<grid, block, 0, s>>>(a); break;
-        default: beam_token_cta_kernel<1><<<grid, block, 0, s>>>(a); break;
+        case 4: return launch_ex(beam_token_cta_kernel<4>, grid, block, 0, s, 1, p, a);
+        case 2: return launch_ex(beam_token_cta_kernel<2>, grid, block, 0, s, 1, p, a);
+        default: return launch_ex(beam_token_cta_kernel<1>, grid, block, 0, s, 1, p, a);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, cudaStream_t s) {
@@ -293,11 +297,8 @@ cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, cudaStream_t s)
     const int rows = beam_bulk_rows(smem_per_sm, a.top_k, a.hidden);
     const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;
     const dim3 grid(static_cast<unsigned>(a.live)), block(a.hidden / 8 / cpt);
-    if (cpt == 2)
-        beam_token_bulk_kernel<2><<<grid, block, bytes, s>>>(a, rows);
-    else
-        beam_token_bulk_kernel<1><<<grid, block, bytes, s>>>(a, rows);
-    return cudaGetLastError();
+    if (cpt == 2) return launch_ex(beam_token_bulk_kernel<2>, grid, block, bytes, s, 1, a.programmatic, a, rows);
+    return launch_ex(beam_token_bulk_kernel<1>, grid, block, bytes, s, 1, a.programmatic, a, rows);
 }
 
 cudaError_t launch_wait_timeout_selftest(unsigned *status, uint64_t timeout_ns, cudaStream_t s) {

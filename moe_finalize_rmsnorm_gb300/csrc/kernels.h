@@ -33,6 +33,7 @@ struct TpArgs {
     int before;                  // weight_before_norm
     unsigned *status;            // device status word
     uint64_t timeout_ns;         // bound of every device-side wait
+    bool programmatic;           // launch with programmatic dependent launch
 };
 
 struct BeamArgs {
@@ -48,6 +49,7 @@ struct BeamArgs {
     int has_norm;
     unsigned *status;
     uint64_t timeout_ns;
+    bool programmatic;
 };
 
 // Per-device one-time set-up (kernel attributes).  `smem_optin` is the

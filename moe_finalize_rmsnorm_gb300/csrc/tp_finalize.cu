@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kChunksPerRow / CPT)
     const int64_t t = blockIdx.x;
     const int tid = threadIdx.x;
 
+    pdl_wait();
     int idx[8];
     float w[8];
     load_route<WK>(a, t, idx, w);
@@ -178,6 +179,7 @@ __global__ void __launch_bounds__(kChunksPerRow / CPT)
     const float r = rsqrtf(__fmaf_rn(tot, 1.0f / kTpHidden, a.eps));
 
     scale_store<CPT, NT>(acc, g, before, r, a.out + t * kTpHidden, tid);
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -195,6 +197,7 @@ __global__ void __launch_bounds__(kChunksPerRow / C) tp_cluster_kernel(const TpA
     const int tid = threadIdx.x;
     const int chunk = static_cast<int>(rank) * NT + tid;
 
+    pdl_wait();
     int idx[8];
     float w[8];
     load_route<WK>(a, t, idx, w);
@@ -239,6 +242,7 @@ __global__ void __launch_bounds__(kChunksPerRow / C) tp_cluster_kernel(const TpA
     const float r = rsqrtf(__fmaf_rn(tot, 1.0f / kTpHidden, a.eps));
 
     scale_store<1, 1>(acc, g, before, r, a.out + t * kTpHidden, chunk);
+    pdl_trigger();
     cluster_barrier();  // no CTA leaves while another may still read its `part`
 }
 
@@ -268,6 +272,7 @@ __global__ void __launch_bounds__(kBulkThreads)
     const uint32_t rows_base = smem_u32(rows_smem);
     const uint32_t bar_addr = smem_u32(&bar);
 
+    pdl_wait();
     int idx[8];
     float w[8];
     load_route<WK>(a, t, idx, w);
@@ -327,6 +332,7 @@ __global__ void __launch_bounds__(kBulkThreads)
     for (int i = 0; i < NW; ++i) tot += red[i];
     const float r = rsqrtf(__fmaf_rn(tot, 1.0f / kTpHidden, a.eps));
     if (ok) scale_store<CPT, NT>(acc, g, before, r, a.out + t * kTpHidden, tid);
+    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -376,6 +382,7 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
     const uint32_t base = smem_u32(rows_smem);
     const uint32_t bar_addr = smem_u32(&bar);
 
+    pdl_wait();
     if (tid < 32) {
         int i = -1;
         float w = 0.f;
@@ -459,6 +466,7 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
         }
         st_cs_16(out_row + static_cast<int64_t>(tid + c * NT) * kChunkElems, pack8_rn(y));
     }
+    pdl_trigger();
 }
 
 // 2 chunks per thread when that leaves at least 256 threads, else 1.
@@ -499,67 +507,51 @@ cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm) {
 cudaError_t launch_tp_token_cta(const TpArgs &a, int wk, cudaStream_t s) {
     constexpr int CPT = 1;
     const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(kChunksPerRow / CPT);
+    const bool p = a.programmatic;
     switch (wk) {
-        case kWeightBF16: tp_token_cta_kernel<CPT, kWeightBF16><<<grid, block, 0, s>>>(a); break;
-        case kWeightPacked: tp_token_cta_kernel<CPT, kWeightPacked><<<grid, block, 0, s>>>(a); break;
-        default: tp_token_cta_kernel<CPT, kWeightFP32><<<grid, block, 0, s>>>(a); break;
-    }
-    return cudaGetLastError();
-}
-
-template <int C>
-static cudaError_t launch_cluster_c(const TpArgs &a, int wk, cudaStream_t s) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.num_tokens * C));
-    cfg.blockDim = dim3(kChunksPerRow / C);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    switch (wk) {
-        case kWeightBF16: return cudaLaunchKernelEx(&cfg, tp_cluster_kernel<C, kWeightBF16>, a);
-        case kWeightPacked: return cudaLaunchKernelEx(&cfg, tp_cluster_kernel<C, kWeightPacked>, a);
-        default: return cudaLaunchKernelEx(&cfg, tp_cluster_kernel<C, kWeightFP32>, a);
+        case kWeightBF16: return launch_ex(tp_token_cta_kernel<CPT, kWeightBF16>, grid, block, 0, s, 1, p, a);
+        case kWeightPacked: return launch_ex(tp_token_cta_kernel<CPT, kWeightPacked>, grid, block, 0, s, 1, p, a);
+        default: return launch_ex(tp_token_cta_kernel<CPT, kWeightFP32>, grid, block, 0, s, 1, p, a);
     }
 }
 
 cudaError_t launch_tp_cluster(const TpArgs &a, int wk, cudaStream_t s) {
-    return launch_cluster_c<8>(a, wk, s);
+    constexpr int C = 8;
+    const dim3 grid(static_cast<unsigned>(a.num_tokens * C)), block(kChunksPerRow / C);
+    const bool p = a.programmatic;
+    switch (wk) {
+        case kWeightBF16: return launch_ex(tp_cluster_kernel<C, kWeightBF16>, grid, block, 0, s, C, p, a);
+        case kWeightPacked: return launch_ex(tp_cluster_kernel<C, kWeightPacked>, grid, block, 0, s, C, p, a);
+        default: return launch_ex(tp_cluster_kernel<C, kWeightFP32>, grid, block, 0, s, C, p, a);
+    }
 }
 
 cudaError_t launch_tp_bulk(const TpArgs &a, int wk, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(kBulkThreads);
+    const bool p = a.programmatic;
     switch (wk) {
-        case kWeightBF16: tp_token_bulk_kernel<kWeightBF16><<<grid, block, kBulkSmem, s>>>(a); break;
-        case kWeightPacked: tp_token_bulk_kernel<kWeightPacked><<<grid, block, kBulkSmem, s>>>(a); break;
-        default: tp_token_bulk_kernel<kWeightFP32><<<grid, block, kBulkSmem, s>>>(a); break;
+        case kWeightBF16: return launch_ex(tp_token_bulk_kernel<kWeightBF16>, grid, block, kBulkSmem, s, 1, p, a);
+        case kWeightPacked: return launch_ex(tp_token_bulk_kernel<kWeightPacked>, grid, block, kBulkSmem, s, 1, p, a);
+        default: return launch_ex(tp_token_bulk_kernel<kWeightFP32>, grid, block, kBulkSmem, s, 1, p, a);
     }
-    return cudaGetLastError();
 }
 
 template <int CPT>
-static void launch_generic_cpt(const TpArgs &a, int wk, int rows, cudaStream_t s) {
+static cudaError_t launch_generic_cpt(const TpArgs &a, int wk, int rows, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(a.hidden / 8 / CPT);
     const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;
+    const bool p = a.programmatic;
     switch (wk) {
-        case kWeightBF16: tp_generic_bulk_kernel<CPT, kWeightBF16><<<grid, block, bytes, s>>>(a, rows); break;
-        case kWeightPacked: tp_generic_bulk_kernel<CPT, kWeightPacked><<<grid, block, bytes, s>>>(a, rows); break;
-        default: tp_generic_bulk_kernel<CPT, kWeightFP32><<<grid, block, bytes, s>>>(a, rows); break;
+        case kWeightBF16: return launch_ex(tp_generic_bulk_kernel<CPT, kWeightBF16>, grid, block, bytes, s, 1, p, a, rows);
+        case kWeightPacked: return launch_ex(tp_generic_bulk_kernel<CPT, kWeightPacked>, grid, block, bytes, s, 1, p, a, rows);
+        default: return launch_ex(tp_generic_bulk_kernel<CPT, kWeightFP32>, grid, block, bytes, s, 1, p, a, rows);
     }
 }
 
 cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, cudaStream_t s) {
     const int rows = generic_rows(smem_per_sm, a.top_k, a.hidden);
-    if (generic_cpt(a.hidden) == 2)
-        launch_generic_cpt<2>(a, wk, rows, s);
-    else
-        launch_generic_cpt<1>(a, wk, rows, s);
-    return cudaGetLastError();
+    if (generic_cpt(a.hidden) == 2) return launch_generic_cpt<2>(a, wk, rows, s);
+    return launch_generic_cpt<1>(a, wk, rows, s);
 }
 
 }  // namespace mf

@@ -50,6 +50,14 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_programmatic_launch_switch(lib):
+    assert lib.mf_get_programmatic_launch() == 1          # on by default
+    lib.mf_set_programmatic_launch(0)
+    assert lib.mf_get_programmatic_launch() == 0
+    lib.mf_set_programmatic_launch(5)
+    assert lib.mf_get_programmatic_launch() == 1
+
+
 def test_status_strings(lib):
     for code in range(9):
         assert lib.mf_status_string(code)

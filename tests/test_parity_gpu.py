@@ -383,3 +383,61 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
     assert cuda_lib.device_status(clear=True) == 0
     case = small_case(8, seed=30)
     compare_bf16(run_tp(cuda_lib, case, "bulk"), oracle_tp(case))
+
+
+# ---------------------------------------------------------------------------
+# programmatic dependent launch
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_programmatic_launch_on_and_off_agree(cuda_lib, variant):
+    case = small_case(300, seed=40)
+    try:
+        cuda_lib.set_programmatic_launch(False)
+        off = run_tp(cuda_lib, case, variant)
+    finally:
+        cuda_lib.set_programmatic_launch(True)
+    on = run_tp(cuda_lib, case, variant)
+    assert np.array_equal(off, on)
+    compare_bf16(on, oracle_tp(case))
+
+
+@pytest.mark.parametrize("variant", ("cluster", "token_cta", "bulk"))
+def test_dependent_calls_see_each_others_output(cuda_lib, variant):
+    # call 1 (Beam finalize without norm, bit-exact with its oracle) writes the
+    # rows that call 2 (finalize + RMSNorm) gathers; both are launched back to
+    # back on one stream with programmatic dependent launch, so call 2 must
+    # wait for call 1.  Expected: the two oracles chained.
+    assert cuda_lib.programmatic_launch()
+    T1, K1 = 64, 4
+    beam = si.beam_case("chain", T1, K1, 4096, T1, routed_scale=1.5, post_weight=False,
+                        post_eps=None, seed=41)
+    x = dev_bf16(beam.expert_outputs)
+    w1 = torch.from_numpy(beam.weights).cuda()
+    mid = torch.empty((T1, 4096), dtype=torch.bfloat16, device="cuda")
+    rng = np.random.default_rng(42)
+    T2 = 48
+    idx2 = rng.integers(-1, T1, size=(T2, 8)).astype(np.int32)
+    w2 = rng.random((T2, 8)).astype(np.float32)
+    nw = f32_bits(rng.standard_normal(4096) * 0.1)
+    out = torch.empty((T2, 4096), dtype=torch.bfloat16, device="cuda")
+    idx2_d, w2_d, nw_d = torch.from_numpy(idx2).cuda(), torch.from_numpy(w2).cuda(), dev_bf16(nw)
+    for _ in range(3):
+        mid.fill_(float("nan"))
+        torch.cuda.synchronize()
+        cuda_lib.beam_moe_finalize(x, w1, mid, beam.routed_scale)
+        cuda_lib.moe_finalize_rmsnorm(mid, w2_d, idx2_d, nw_d, out, eps=1e-6, gain_center=1.0,
+                                      weight_before_norm=True, variant=variant)
+        torch.cuda.synchronize()
+        got = host_bits(out)
+        assert not np.isnan(bf16_bits_to_f64(got)).any(), "call 2 read call 1's output too early"
+    ref1 = oracle_beam(beam)
+    assert np.array_equal(host_bits(mid), ref1)
+    ref2 = oracle.moe_finalize_rmsnorm(ref1, w2, idx2, nw, eps=1e-6, gain_center=1.0,
+                                       weight_before_norm=True)
+    compare_bf16(got, ref2)
+
+
+def f32_bits(a):
+    u = np.asarray(a, dtype=np.float32).view(np.uint32).copy()
+    u += ((u >> 16) & np.uint32(1)) + np.uint32(0x7FFF)
+    return (u >> 16).astype(np.uint16)
