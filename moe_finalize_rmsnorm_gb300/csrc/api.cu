@@ -5,7 +5,7 @@
 #include <atomic>
 #include <mutex>
 
-#include "../../include/moe_finalize.h"
+#include "moe_finalize.h"
 #include "common.cuh"
 #include "kernels.h"
 
