@@ -441,3 +441,40 @@ def f32_bits(a):
     u = np.asarray(a, dtype=np.float32).view(np.uint32).copy()
     u += ((u >> 16) & np.uint32(1)) + np.uint32(0x7FFF)
     return (u >> 16).astype(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# CUDA graphs: calls captured once (after a first call outside capture) and
+# replayed with new inputs written into the captured buffers
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_graph_replay_with_new_inputs(cuda_lib, variant):
+    cases = [small_case(200, seed=50), small_case(200, seed=51)]
+    a = cases[0]
+    g = dev_bf16(a.gemm2)
+    w = torch.from_numpy(a.weights).cuda()
+    idx = torch.from_numpy(a.idx).cuda()
+    nw = dev_bf16(a.norm_weight)
+    out = torch.empty((200, 4096), dtype=torch.bfloat16, device="cuda")
+
+    def call():
+        cuda_lib.moe_finalize_rmsnorm(g, w, idx, nw, out, eps=a.eps, gain_center=a.gain_center,
+                                      weight_before_norm=a.weight_before_norm, variant=variant)
+
+    call()                                   # first call outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s), torch.cuda.graph(graph, stream=s):
+        call()
+    torch.cuda.synchronize()
+    for c in cases:
+        g.copy_(dev_bf16(c.gemm2))
+        w.copy_(torch.from_numpy(c.weights).cuda())
+        idx.copy_(torch.from_numpy(c.idx).cuda())
+        nw.copy_(dev_bf16(c.norm_weight))
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        compare_bf16(host_bits(out), oracle_tp(c))
