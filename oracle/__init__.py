@@ -12,6 +12,11 @@ Every function follows the pages:
   (API page: description and parameter list).
 * ``beam_moe_finalize`` -- vllm.models.beam.nvidia.moe_finalize,
   beam_moe_finalize (docstring and source).
+* ``beam_moe_finalize_norm_residual_norm`` -- vllm.models.beam.nvidia.
+  moe_finalize, beam_moe_finalize_norm_residual_norm: Beam finalize, then the
+  residual step of its unfused reference.  PARTLY UNPINNED: the residual step
+  (beam_norm_residual_norm) is not on the pages; it is read as
+  hidden = BF16(s0 x + s1 residual) in FP32 and normalized = BF16(RMSNorm(hidden)).
 * ``bf16_from_double`` -- the BF16 format itself (upper half of binary32),
   round-to-nearest-even.
 
@@ -66,6 +71,9 @@ def _load():
             lib.oracle_beam_moe_finalize.argtypes = [
                 vp, vp, vp, i64, i32, i32, f32, vp, f32, c_int]
             lib.oracle_beam_moe_finalize.restype = c_int
+            lib.oracle_beam_moe_finalize_norm_residual_norm.argtypes = [
+                vp, vp, vp, i64, i32, i32, f32, vp, f32, c_int, vp, f32, c_int, f32, f32, vp, vp]
+            lib.oracle_beam_moe_finalize_norm_residual_norm.restype = c_int
             _lib = lib
     return _lib
 
@@ -147,3 +155,38 @@ def beam_moe_finalize(expert_outputs: np.ndarray, weights: np.ndarray, live_toke
     if rc != 0:
         raise MemoryError("oracle could not allocate its row buffers")
     return out
+
+
+def beam_moe_finalize_norm_residual_norm(
+        expert_outputs: np.ndarray, weights: np.ndarray, residual: np.ndarray, *,
+        routed_scale: float = 1.0, post_weight: np.ndarray | None = None,
+        post_eps: float | None = None, next_weight: np.ndarray | None = None,
+        next_eps: float | None = None,
+        scales: tuple[float, float] | None = None) -> tuple[np.ndarray, np.ndarray | None]:
+    """Oracle of beam_moe_finalize_norm_residual_norm (partly unpinned).
+
+    expert_outputs: uint16 [capacity, top_k, hidden]; weights: float32
+    [>= tokens, top_k]; residual: uint16 [tokens, hidden] (tokens = live rows).
+    Returns (hidden, normalized); normalized is None without next_eps.
+    """
+    assert expert_outputs.dtype == np.uint16 and expert_outputs.ndim == 3
+    cap, k, hidden = expert_outputs.shape
+    assert residual.dtype == np.uint16 and residual.ndim == 2 and residual.shape[1] == hidden
+    tokens = residual.shape[0]
+    assert tokens <= cap and weights.dtype == np.float32 and weights.shape[0] >= tokens
+    for w, e in ((post_weight, post_eps), (next_weight, next_eps)):
+        if w is not None:
+            assert e is not None and w.shape == (hidden,) and w.dtype == np.uint16
+    s0, s1 = scales if scales is not None else (1.0, 1.0)
+    hid = np.empty((tokens, hidden), dtype=np.uint16)
+    norm = np.empty((tokens, hidden), dtype=np.uint16) if next_eps is not None else None
+    if tokens == 0:
+        return hid, norm
+    rc = _load().oracle_beam_moe_finalize_norm_residual_norm(
+        _ptr(expert_outputs), _ptr(weights), _ptr(residual), tokens, k, hidden,
+        float(routed_scale), _ptr(post_weight), float(post_eps or 0.0), int(post_eps is not None),
+        _ptr(next_weight), float(next_eps or 0.0), int(next_eps is not None), float(s0),
+        float(s1), _ptr(hid), _ptr(norm))
+    if rc != 0:
+        raise MemoryError("oracle could not allocate its row buffers")
+    return hid, norm

@@ -36,6 +36,19 @@
  * reduction" on a BF16 tensor is read as PyTorch's BF16-tensor-times-scalar:
  * an FP32 product rounded to BF16.
  *
+ *   vllm.models.beam.nvidia.moe_finalize, beam_moe_finalize_norm_residual_norm
+ *   (docstring and source): the Beam finalize above (with its optional post
+ *   norm) followed, for the same live rows, by the residual step of the unfused
+ *   reference, beam_norm_residual_norm(finalized, residual, None, None,
+ *   next_weight, next_eps, scales).  That function is not shown on the pages,
+ *   so this step is PARTLY UNPINNED; it is read as
+ *     hidden     = BF16(s0 * finalized + s1 * residual)   FP32: one product,
+ *                  then one fused multiply-add, scales (s0, s1) = (1, 1) when
+ *                  none are given
+ *     normalized = BF16(hidden / sqrt(mean(hidden^2) + next_eps) * next_weight)
+ *                  (float64, unweighted when next_weight is absent), only when
+ *                  next_eps is given.
+ *
  * Readings where the pages are silent:
  *   - eps sits inside the square root (standard RMSNorm), for both ops;
  *   - "out of range" means i >= rows (rows = gemm2_permuted.shape[0]);
@@ -233,6 +246,58 @@ int oracle_beam_moe_finalize(const uint16_t *expert_outputs, const float *weight
         }
     }
     free(acc);
+    free(v);
+    return 0;
+}
+
+/*
+ * beam_moe_finalize_norm_residual_norm for tokens [0, tokens) (partly
+ * unpinned: see the header comment).
+ *
+ * expert_outputs, weights, post_weight, post_eps, has_post_norm: as for
+ * oracle_beam_moe_finalize.  residual: BF16 bits [tokens, hidden].
+ * next_weight: BF16 bits [hidden] or NULL.  hidden_out: BF16 bits [tokens,
+ * hidden].  normalized_out: BF16 bits [tokens, hidden], written only when
+ * has_next_norm.  Returns 0, or -1 if a row buffer could not be allocated.
+ */
+int oracle_beam_moe_finalize_norm_residual_norm(
+    const uint16_t *expert_outputs, const float *weights, const uint16_t *residual, int64_t tokens,
+    int32_t top_k, int32_t hidden, float routed_scale, const uint16_t *post_weight, float post_eps,
+    int has_post_norm, const uint16_t *next_weight, float next_eps, int has_next_norm,
+    float scale_x, float scale_residual, uint16_t *hidden_out, uint16_t *normalized_out)
+{
+    uint16_t *finalized = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)hidden);
+    double *v = (double *)malloc(sizeof(double) * (size_t)hidden);
+    if (!finalized || !v) {
+        free(finalized);
+        free(v);
+        return -1;
+    }
+    for (int64_t t = 0; t < tokens; ++t) {
+        if (oracle_beam_moe_finalize(expert_outputs + t * top_k * (int64_t)hidden,
+                                     weights + t * top_k, finalized, 1, top_k, hidden, routed_scale,
+                                     post_weight, post_eps, has_post_norm) != 0) {
+            free(finalized);
+            free(v);
+            return -1;
+        }
+        for (int32_t h = 0; h < hidden; ++h) {
+            float x = bf16_bits_to_float(finalized[h]);
+            float r = bf16_bits_to_float(residual[t * hidden + h]);
+            float sum = fmaf(scale_residual, r, scale_x * x);
+            uint16_t b = oracle_bf16_from_double((double)sum);
+            hidden_out[t * hidden + h] = b;
+            v[h] = bf16_bits_to_double(b);
+        }
+        if (!has_next_norm)
+            continue;
+        double rs = inverse_rms(v, hidden, (double)next_eps);
+        for (int32_t h = 0; h < hidden; ++h) {
+            double gamma = next_weight ? bf16_bits_to_double(next_weight[h]) : 1.0;
+            normalized_out[t * hidden + h] = oracle_bf16_from_double(v[h] * rs * gamma);
+        }
+    }
+    free(finalized);
     free(v);
     return 0;
 }

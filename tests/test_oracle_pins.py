@@ -529,3 +529,84 @@ def test_beam_reduction_equals_tp_gather_with_identity_map():
     tp_scaled = bf16_bits_to_f64(tp) * 2.0 ** 20
     compare_bf16(f64_to_bf16_bits(tp_scaled), beam, min_exact=0.99)
     assert math.isfinite(float(tp_scaled.max()))
+
+
+# --------------------------------------------------------------------------
+# beam_moe_finalize_norm_residual_norm (the residual step is partly unpinned:
+# hidden = BF16(s0 x + s1 residual) in FP32, normalized = BF16(RMSNorm(hidden)))
+
+def _identity_beam(values):
+    """expert_outputs with top_k 1 holding `values`, unit weights: the Beam
+    finalize (scale 1, no norm) returns them unchanged."""
+    x = bits([[list(v)] for v in values])
+    return x, np.ones((x.shape[0], 1), dtype=np.float32)
+
+
+def test_residual_add_hand_example():
+    # x + r with scales (1, 1): 1.5 + 0.25 = 1.75; 1 + 2^-8 is a tie -> 1 (even);
+    # -2 + 0.5 = -1.5; 3 - 3 = 0
+    x, w = _identity_beam([[1.5, 1.0, -2.0, 3.0]])
+    r = bits([[0.25, 2 ** -8, 0.5, -3.0]])
+    hid, norm = oracle.beam_moe_finalize_norm_residual_norm(x, w, r)
+    assert norm is None
+    assert vals(hid[0]) == [1.75, 1.0, -1.5, 0.0]
+
+
+def test_residual_scales_hand_example():
+    # scales (2, 0.5): 2*1.5 + 0.5*1 = 3.5, 2*1 + 0.5*2 = 3, 2*-2 + 0.5*4 = -2,
+    # 2*3 + 0.5*-8 = 2
+    x, w = _identity_beam([[1.5, 1.0, -2.0, 3.0]])
+    r = bits([[1.0, 2.0, 4.0, -8.0]])
+    hid, _ = oracle.beam_moe_finalize_norm_residual_norm(x, w, r, scales=(2.0, 0.5))
+    assert vals(hid[0]) == [3.5, 3.0, -2.0, 2.0]
+
+
+def test_residual_next_norm_closed_form():
+    # hidden = 0.5 + 0.5 = 1 everywhere; next norm with eps 3: 1/sqrt(1+3) = 0.5,
+    # times next_weight [2, 1, -1, 0.5] -> [1, 0.5, -0.5, 0.25]
+    x, w = _identity_beam([[0.5] * 4, [0.5] * 4])
+    r = bits([[0.5] * 4, [0.5] * 4])
+    hid, norm = oracle.beam_moe_finalize_norm_residual_norm(
+        x, w, r, next_weight=bits([2.0, 1.0, -1.0, 0.5]), next_eps=3.0)
+    assert np.all(hid == 0x3F80)
+    assert vals(norm[0]) == vals(norm[1]) == [1.0, 0.5, -0.5, 0.25]
+
+
+def test_residual_zero_reduces_to_beam_and_library_rmsnorm():
+    # residual 0 and scales (1, 1): hidden is the Beam finalize output bit for
+    # bit, and normalized is PyTorch's float64 rms_norm of it
+    rng = np.random.default_rng(60)
+    cap, K, H, T = 6, 4, 1024, 5
+    x = f32_to_bf16_bits(rng.standard_normal((cap, K, H)).astype(np.float32))
+    w = rng.random((cap, K)).astype(np.float32)
+    pw = f32_to_bf16_bits((1 + 0.05 * rng.standard_normal(H)).astype(np.float32))
+    nw = f32_to_bf16_bits((1 + 0.1 * rng.standard_normal(H)).astype(np.float32))
+    r = np.zeros((T, H), dtype=np.uint16)
+    hid, norm = oracle.beam_moe_finalize_norm_residual_norm(
+        x, w, r, routed_scale=2.5, post_weight=pw, post_eps=1e-6, next_weight=nw, next_eps=1e-5)
+    beam = oracle.beam_moe_finalize(x, w, T, routed_scale=2.5, post_weight=pw, post_eps=1e-6)
+    assert np.array_equal(hid, beam)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(bf16_bits_to_f64(hid)), (H,),
+                                       torch.from_numpy(bf16_bits_to_f64(nw)), 1e-5)
+    compare_bf16(norm, ref.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16),
+                 min_exact=0.999)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_residual_matches_float64_brute_force(seed):
+    rng = np.random.default_rng(70 + seed)
+    cap, K, H = 7, [1, 5, 8][seed], [256, 768, 2048][seed]
+    T = int(rng.integers(1, cap + 1))
+    x = f32_to_bf16_bits(rng.standard_normal((cap, K, H)).astype(np.float32))
+    w = rng.random((cap, K)).astype(np.float32)
+    res = f32_to_bf16_bits(rng.standard_normal((T, H)).astype(np.float32))
+    nw = f32_to_bf16_bits((1 + 0.1 * rng.standard_normal(H)).astype(np.float32))
+    s0, s1 = [(1.0, 1.0), (0.5, 2.0), (1.25, -0.75)][seed]
+    hid, norm = oracle.beam_moe_finalize_norm_residual_norm(
+        x, w, res, routed_scale=1.0, next_weight=nw, next_eps=1e-6, scales=(s0, s1))
+    fin = _brute_beam(x, w, T, 1.0, None, None)
+    h = s0 * bf16_bits_to_f64(fin) + s1 * bf16_bits_to_f64(res)
+    compare_bf16(hid, f64_to_bf16_bits(h), min_exact=0.99)
+    hv = bf16_bits_to_f64(hid)
+    y = hv / np.sqrt((hv * hv).mean(axis=1, keepdims=True) + 1e-6) * bf16_bits_to_f64(nw)
+    compare_bf16(norm, f64_to_bf16_bits(y), min_exact=0.99)
