@@ -10,7 +10,8 @@ alternates between steps so both orderings are timed.  The inputs (2.42 GB
 per call) are larger than L2, so every call reads its rows from HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload roofline|padded|beam|small|decode|custom] [--tokens T]
+                    [--workload roofline|padded|beam|beam_residual|small|decode|custom]
+                    [--tokens T]
                     [--hidden H --top-k K --weights fp32|bf16|packed]
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle (the
@@ -250,6 +251,29 @@ def make_beam_job(torch, mf, case: si.BeamCase, device, variant: str) -> Job:
     return job
 
 
+def make_beam_residual_job(torch, mf, case: si.BeamCase, device) -> Job:
+    """Beam finalize + residual add + next RMSNorm over the live rows."""
+    cap, K, H = case.expert_outputs.shape
+    T = case.live_tokens
+    x = _dev_bf16(torch, case.expert_outputs.reshape(cap * K, H), device)
+    w = torch.from_numpy(case.weights).to(device)
+    pw = _dev_bf16(torch, case.post_weight, device)
+    res = _dev_bf16(torch, case.meta["residual"], device)
+    nw = _dev_bf16(torch, case.meta["next_weight"], device)
+    hid = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    nrm = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+
+    def launch(step: int, tensors=(x, w, res, pw, nw, hid, nrm)):
+        xx, ww, rr, pp, nn, hh, oo = tensors
+        mf.beam_moe_finalize_norm_residual_norm(xx, ww, rr, pp, case.post_eps, nn, 1e-6, None,
+                                                case.routed_scale, hidden=hh, normalized=oo)
+
+    job = Job(case.name + "_residual", T, si.algorithmic_bytes_beam_residual(T, H, K, True),
+              "beam_token_bulk_kernel", launch, case, {"variant": "bulk"})
+    job.device_tensors = (x, w, res, pw, nw, hid, nrm)
+    return job
+
+
 def workload_case(name: str, tokens: int | None, seed_rank: int, args_hidden: int = 4096,
                   args_top_k: int = 8, args_weights: str = "fp32"):
     """Host inputs of a named workload (rank-dependent seed for N > 1)."""
@@ -278,6 +302,14 @@ def workload_case(name: str, tokens: int | None, seed_rank: int, args_hidden: in
                        gain_center=1.0, eps=1e-6, seed=seed_rank)
         return "tp", c, (f"finalize+RMSNorm num_tokens={T} hidden={H} top_k={K} "
                          f"{args_weights} weights, 1% invalid, rows={T * K} ~N(0,1)")
+    if name == "beam_residual":
+        c = si.beam_8000_live(poison_dead_rows=False)
+        c.meta["residual"] = si.normal_bf16((c.live_tokens, 7168), 1.0, 7, 1)
+        c.meta["next_weight"] = si.normal_bf16((7168,), 0.1, 8, 1, mu=1.0)
+        return "beam_residual", c, (
+            "Beam finalize + residual add + next RMSNorm: capacity=8192 top_k=8 hidden=7168 "
+            "tokens=8000 routed_scale=2.5 post-RMSNorm, residual ~N(0,1), next_weight "
+            "~1+N(0,0.1), next_eps=1e-6")
     if name == "beam":
         return "beam", si.beam_8000_live(poison_dead_rows=False), (
             "Beam finalize capacity=8192 top_k=8 hidden=7168 live_tokens=8000 routed_scale=2.5 "
@@ -307,6 +339,13 @@ def time_oracle(kind: str, case, token_lo: int, token_hi: int, threads: int,
                 gain_center=case.gain_center,
                 weight_before_norm=case.weight_before_norm if before is None else before,
                 hidden=case.hidden)
+        elif kind == "beam_residual":
+            oracle.beam_moe_finalize_norm_residual_norm(
+                np.ascontiguousarray(case.expert_outputs[lo:hi]),
+                np.ascontiguousarray(case.weights[lo:hi]),
+                np.ascontiguousarray(case.meta["residual"][lo:hi]),
+                routed_scale=case.routed_scale, post_weight=case.post_weight,
+                post_eps=case.post_eps, next_weight=case.meta["next_weight"], next_eps=1e-6)
         else:
             oracle.beam_moe_finalize(
                 np.ascontiguousarray(case.expert_outputs[lo:hi]),
@@ -400,6 +439,8 @@ def run_ours(args) -> None:
     if kind == "tp":
         job = make_tp_job(torch, mf, case, device, args.variant,
                           alternate=args.workload == "roofline")
+    elif kind == "beam_residual":
+        job = make_beam_residual_job(torch, mf, case, device)
     else:
         job = make_beam_job(torch, mf, case, device, args.variant)
     stream = torch.cuda.current_stream(device)
@@ -558,7 +599,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="roofline",
-                   choices=("roofline", "padded", "beam", "small", "decode", "custom"))
+                   choices=("roofline", "padded", "beam", "beam_residual", "small", "decode",
+                            "custom"))
     p.add_argument("--tokens", type=int, default=None,
                    help="token count of --workload decode / custom")
     p.add_argument("--hidden", type=int, default=4096, help="hidden size of --workload custom")

@@ -189,6 +189,47 @@ mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity
                                     float post_eps, int has_post_norm, mf_variant variant,
                                     mf_stream_t stream);
 
+/*
+ * beam_moe_finalize_norm_residual_norm -- vllm.models.beam.nvidia.moe_finalize,
+ * beam_moe_finalize_norm_residual_norm (docstring: "finalize local MegaMoE
+ * tokens through the next normalization boundary"; source: the assertions and
+ * the unfused reference), on one GPU.  For each of the first `tokens` rows:
+ *
+ *   f          = the beam_moe_finalize result for the row (above), including
+ *                its optional post-RMSNorm, rounded to BF16
+ *   hidden     = BF16(scale_x * f + scale_residual * residual)   FP32: one
+ *                product, one fused multiply-add
+ *   normalized = BF16(hidden / sqrt(mean(hidden^2) + next_eps) * next_weight)
+ *                when has_next_norm (unweighted if next_weight is NULL)
+ *
+ * The residual step stands for the unfused reference's call
+ * beam_norm_residual_norm(finalized, residual, None, None, next_weight,
+ * next_eps, scales), whose body the pages do not show: this reading of it
+ * (scales = (scale_x, scale_residual), (1, 1) when the caller has none) is
+ * partly unpinned.
+ *
+ *   expert_outputs, capacity, expert_weights, weight_rows, top_k, hidden,
+ *   routed_scale, post_weight, post_eps, has_post_norm: as for beam_moe_finalize,
+ *                    with tokens in place of live_tokens.
+ *   residual         device BF16 [tokens, hidden] contiguous, 16-byte aligned.
+ *   tokens           0 <= tokens <= capacity, weight_rows >= tokens.
+ *   next_weight      device BF16 [hidden] (16-byte aligned) or NULL; needs has_next_norm.
+ *   hidden_out       device BF16 [tokens, hidden], 16-byte aligned; may be the
+ *                    residual buffer itself (an in-place residual update).
+ *   normalized_out   device BF16 [tokens, hidden], 16-byte aligned, required
+ *                    when has_next_norm and NULL otherwise.
+ *
+ * Errors: MF_ERR_UNSUPPORTED, MF_ERR_SHAPE, MF_ERR_INVALID (a weight without
+ * its norm flag, normalized_out without has_next_norm), MF_ERR_NULL,
+ * MF_ERR_ALIGN, MF_ERR_CUDA.  Zero tokens: MF_OK, nothing launched.
+ */
+mf_status beam_moe_finalize_norm_residual_norm(
+    const void *expert_outputs, int64_t capacity, const float *expert_weights, int64_t weight_rows,
+    const void *residual, int64_t tokens, int32_t top_k, int32_t hidden, float routed_scale,
+    const void *post_weight, float post_eps, int has_post_norm, const void *next_weight,
+    float next_eps, int has_next_norm, float scale_x, float scale_residual, void *hidden_out,
+    void *normalized_out, mf_stream_t stream);
+
 /* The kernel AUTO would run for moe_finalize_rmsnorm with these sizes
  * (MF_VARIANT_AUTO if none would run: no tokens or unsupported sizes).  Sizes
  * other than 4096 / 8 always run the generic bulk-staged kernel (MF_VARIANT_BULK). */

@@ -10,6 +10,8 @@ streams.  There is no CPU fallback: without the built library the calls raise.
   flashinfer.comm.tp_moe_finalize_rmsnorm (API page), on one GPU.
 * ``beam_moe_finalize`` follows vllm.models.beam.nvidia.moe_finalize,
   beam_moe_finalize.
+* ``beam_moe_finalize_norm_residual_norm`` follows the same page's function of
+  that name on one GPU (its residual step is a reading; see the C header).
 """
 from __future__ import annotations
 
@@ -21,7 +23,8 @@ from ._abi import (MF_DTYPE_BF16, MF_DTYPE_FP32, MF_DTYPE_PACKED_TOPK, VARIANT_N
                    check, lib)
 
 __all__ = [
-    "moe_finalize_rmsnorm", "tp_moe_finalize_rmsnorm", "beam_moe_finalize", "MoeFinalizeError",
+    "moe_finalize_rmsnorm", "tp_moe_finalize_rmsnorm", "beam_moe_finalize",
+    "beam_moe_finalize_norm_residual_norm", "MoeFinalizeError",
     "device_status", "selftest_wait_timeout", "select_finalize_variant", "select_beam_variant",
     "version", "set_programmatic_launch", "programmatic_launch", "HIDDEN", "TOP_K",
 ]
@@ -131,6 +134,64 @@ def beam_moe_finalize(expert_outputs: torch.Tensor, expert_weights: torch.Tensor
             int(post_eps is not None), _variant(variant), _stream_ptr(stream, dev))
     check(st, "beam_moe_finalize")
     return out
+
+
+def beam_moe_finalize_norm_residual_norm(
+        gemm2_permuted: torch.Tensor, expert_weights: torch.Tensor, residual: torch.Tensor,
+        post_weight: torch.Tensor | None, post_eps: float | None,
+        next_weight: torch.Tensor | None, next_eps: float | None,
+        scales: tuple[float, float] | None, routed_scale: float = 1.0, *,
+        hidden: torch.Tensor | None = None, normalized: torch.Tensor | None = None,
+        stream: torch.cuda.Stream | None = None) -> tuple[torch.Tensor, torch.Tensor | None]:
+    """Beam finalize of the first ``residual.shape[0]`` tokens, then the residual
+    add and the next RMSNorm, in one kernel.  Returns ``(hidden, normalized)``;
+    ``normalized`` is None without ``next_eps``.
+
+    gemm2_permuted: contiguous BF16 [capacity * top_k, hidden] token-major rows
+    (or [capacity, top_k, hidden]); expert_weights: FP32 [capacity, top_k];
+    residual: BF16 [tokens, hidden].  hidden = BF16(s0 * finalized + s1 *
+    residual) with scales (s0, s1), (1, 1) when None; ``hidden`` may be
+    ``residual`` itself.
+    """
+    w, r = expert_weights, residual
+    _req(w.dim() == 2 and w.dtype == torch.float32 and w.is_contiguous(),
+         "expert_weights must be a contiguous 2-D FP32 tensor")
+    cap, top_k = w.shape
+    _req(r.dim() == 2 and r.dtype == torch.bfloat16 and r.is_contiguous(),
+         "residual must be a contiguous 2-D BF16 tensor")
+    tokens, hid_size = r.shape
+    x = gemm2_permuted
+    _req(x.dtype == torch.bfloat16 and x.is_contiguous() and x.numel() == cap * top_k * hid_size,
+         "gemm2_permuted must be contiguous BF16 [capacity * top_k, hidden]")
+    dev = r.device
+    _req(dev.type == "cuda" and x.device == dev and w.device == dev,
+         "all tensors must be on the same CUDA device")
+    for wt, eps in ((post_weight, post_eps), (next_weight, next_eps)):
+        if wt is not None:
+            _req(eps is not None, "a norm weight requires its eps")
+            _req(wt.shape == (hid_size,) and wt.is_contiguous() and wt.dtype == torch.bfloat16
+                 and wt.device == dev, "norm weights must be contiguous BF16 [hidden]")
+    if hidden is None:
+        hidden = torch.empty_like(r)
+    if normalized is None and next_eps is not None:
+        normalized = torch.empty_like(r)
+    if next_eps is None:
+        normalized = None
+    for o in (hidden, normalized):
+        if o is not None:
+            _req(o.shape == r.shape and o.dtype == torch.bfloat16 and o.is_contiguous() and
+                 o.device == dev, "outputs must be contiguous BF16 like residual")
+    s0, s1 = scales if scales is not None else (1.0, 1.0)
+    with torch.cuda.device(dev):
+        st = lib().beam_moe_finalize_norm_residual_norm(
+            x.data_ptr(), cap, w.data_ptr(), cap, r.data_ptr(), tokens, top_k, hid_size,
+            float(routed_scale), None if post_weight is None else post_weight.data_ptr(),
+            float(post_eps or 0.0), int(post_eps is not None),
+            None if next_weight is None else next_weight.data_ptr(), float(next_eps or 0.0),
+            int(next_eps is not None), float(s0), float(s1), hidden.data_ptr(),
+            None if normalized is None else normalized.data_ptr(), _stream_ptr(stream, dev))
+    check(st, "beam_moe_finalize_norm_residual_norm")
+    return hidden, normalized
 
 
 def select_finalize_variant(num_tokens: int, hidden: int = HIDDEN, top_k: int = TOP_K) -> str:

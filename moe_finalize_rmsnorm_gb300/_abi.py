@@ -29,6 +29,9 @@ SIGNATURES = {
     "moe_finalize_rmsnorm_variant": (_int, _TP_ARGS + [_int, _vp]),
     "beam_moe_finalize": (_int, _BEAM_ARGS + [_vp]),
     "beam_moe_finalize_variant": (_int, _BEAM_ARGS + [_int, _vp]),
+    "beam_moe_finalize_norm_residual_norm": (
+        _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i32, _i32, _f32, _vp, _f32, _int, _vp, _f32,
+               _int, _f32, _f32, _vp, _vp, _vp]),
     "mf_select_finalize_variant": (_int, [_i64, _i32, _i32]),
     "mf_select_beam_variant": (_int, [_i64, _i32, _i32]),
     "mf_status_string": (ctypes.c_char_p, [_int]),

@@ -139,7 +139,7 @@ mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
     mf_status st = device_info(&d);
     if (st != MF_OK) return st;
 
-    mf::TpArgs a;
+    mf::TpArgs a = {};
     a.gemm2 = static_cast<const uint16_t *>(gemm2_permuted);
     a.rows = rows;
     a.ld = row_stride;
@@ -208,7 +208,7 @@ mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity
     mf_status st = device_info(&d);
     if (st != MF_OK) return st;
 
-    mf::BeamArgs a;
+    mf::BeamArgs a = {};
     a.x = static_cast<const uint16_t *>(expert_outputs);
     a.weights = expert_weights;
     a.out = static_cast<uint16_t *>(output);
@@ -225,7 +225,8 @@ mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     if (variant == MF_VARIANT_AUTO) variant = pick_beam(live_tokens);
-    if (variant == MF_VARIANT_BULK) return from_launch(mf::launch_beam_bulk(a, d->smem_per_sm, s));
+    if (variant == MF_VARIANT_BULK)
+        return from_launch(mf::launch_beam_bulk(a, d->smem_per_sm, false, s));
     return from_launch(mf::launch_beam_token_cta(a, s));
 }
 
@@ -237,6 +238,58 @@ mf_status beam_moe_finalize(const void *expert_outputs, int64_t capacity,
     return beam_moe_finalize_variant(expert_outputs, capacity, expert_weights, weight_rows, output,
                                      live_tokens, top_k, hidden, routed_scale, post_weight,
                                      post_eps, has_post_norm, MF_VARIANT_AUTO, stream);
+}
+
+mf_status beam_moe_finalize_norm_residual_norm(
+    const void *expert_outputs, int64_t capacity, const float *expert_weights, int64_t weight_rows,
+    const void *residual, int64_t tokens, int32_t top_k, int32_t hidden, float routed_scale,
+    const void *post_weight, float post_eps, int has_post_norm, const void *next_weight,
+    float next_eps, int has_next_norm, float scale_x, float scale_residual, void *hidden_out,
+    void *normalized_out, mf_stream_t stream) {
+    if (top_k < 1 || top_k > 32) return MF_ERR_UNSUPPORTED;
+    if (hidden < 256 || hidden > 8192 || hidden % 256 != 0) return MF_ERR_UNSUPPORTED;
+    if (capacity < 0 || tokens < 0 || tokens > capacity || weight_rows < tokens)
+        return MF_ERR_SHAPE;
+    if ((post_weight && !has_post_norm) || (next_weight && !has_next_norm) ||
+        (normalized_out && !has_next_norm))
+        return MF_ERR_INVALID;
+    if (tokens == 0) return MF_OK;
+    if (!expert_outputs || !expert_weights || !residual || !hidden_out ||
+        (has_next_norm && !normalized_out))
+        return MF_ERR_NULL;
+    if (!aligned(expert_outputs, 16) || !aligned(residual, 16) || !aligned(hidden_out, 16) ||
+        !aligned(expert_weights, 4) || (normalized_out && !aligned(normalized_out, 16)) ||
+        (post_weight && !aligned(post_weight, 16)) || (next_weight && !aligned(next_weight, 16)))
+        return MF_ERR_ALIGN;
+    if (tokens > 0x7fffffffLL) return MF_ERR_SHAPE;
+
+    const DeviceInfo *d = nullptr;
+    mf_status st = device_info(&d);
+    if (st != MF_OK) return st;
+
+    mf::BeamArgs a = {};
+    a.x = static_cast<const uint16_t *>(expert_outputs);
+    a.weights = expert_weights;
+    a.out = static_cast<uint16_t *>(hidden_out);
+    a.post_weight = static_cast<const uint16_t *>(post_weight);
+    a.live = tokens;
+    a.top_k = top_k;
+    a.hidden = hidden;
+    a.routed_scale = routed_scale;
+    a.post_eps = post_eps;
+    a.has_norm = has_post_norm ? 1 : 0;
+    a.status = d->status;
+    a.timeout_ns = kWaitLimitNs;
+    a.programmatic = g_programmatic.load() != 0;
+    a.residual = static_cast<const uint16_t *>(residual);
+    a.next_weight = static_cast<const uint16_t *>(next_weight);
+    a.normalized = static_cast<uint16_t *>(normalized_out);
+    a.next_eps = next_eps;
+    a.has_next = has_next_norm ? 1 : 0;
+    a.scale_x = scale_x;
+    a.scale_residual = scale_residual;
+    return from_launch(mf::launch_beam_bulk(a, d->smem_per_sm, true,
+                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
 mf_variant mf_select_finalize_variant(int64_t num_tokens, int32_t hidden, int32_t top_k) {

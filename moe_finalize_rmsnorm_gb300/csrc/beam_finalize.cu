@@ -145,6 +145,67 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
     pdl_trigger();
 }
 
+// Residual step of beam_moe_finalize_norm_residual_norm: the finalized value
+// f = BF16(v * rs * post_weight) (or v), then hidden = BF16(s0 f + s1 residual)
+// in FP32 (one product, one FMA), stored; with the next norm, normalized =
+// BF16(hidden * rsqrt(mean(hidden^2) + next_eps) * next_weight).  Each thread
+// reads the residual chunks it then overwrites, so hidden may be written into
+// the residual buffer itself.
+template <int CPT>
+__device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const BeamArgs &a, bool norm,
+                                                  float rs, int64_t t, int tid, int NT, float *red,
+                                                  bool ok) {
+    const int H = a.hidden;
+    const uint16_t *res_row = a.residual + t * H;
+    uint16_t *hid_row = a.out + t * H;
+    float ss = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+        const int chunk = tid + c * NT;
+        float r[8];
+        unpack8(ld_nc_na_16(res_row + static_cast<int64_t>(chunk) * kChunkElems), r);
+        float pw[8];
+        if (norm && a.post_weight) {
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(a.post_weight) + chunk), pw);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) pw[j] = 1.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float f = norm ? round_bf16(__fmul_rn(__fmul_rn(v[c][j], rs), pw[j])) : v[c][j];
+            const float h = round_bf16(__fmaf_rn(a.scale_residual, r[j], __fmul_rn(a.scale_x, f)));
+            v[c][j] = h;
+            ss = __fmaf_rn(h, h, ss);
+        }
+        if (ok) st_cs_16(hid_row + static_cast<int64_t>(chunk) * kChunkElems, pack8_rn(v[c]));
+    }
+    if (!a.has_next) return;
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) red[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    const int nw = NT >> 5;
+    for (int i = 0; i < nw; ++i) tot += red[i];
+    const float rn = inv_rms(tot, H, a.next_eps);
+    uint16_t *norm_row = a.normalized + t * H;
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) {
+        const int chunk = tid + c * NT;
+        float g[8];
+        if (a.next_weight) {
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(a.next_weight) + chunk), g);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) g[j] = 1.f;
+        }
+        float y[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(__fmul_rn(v[c][j], rn), g[j]);
+        if (ok) st_cs_16(norm_row + static_cast<int64_t>(chunk) * kChunkElems, pack8_rn(y));
+    }
+}
+
 // ---------------------------------------------------------------------------
 // one CTA per live token, the token's rows staged in shared memory
 
@@ -154,12 +215,13 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
 // no registers, and two CTAs per SM keep two tokens' blocks in flight while
 // one of them reduces.  Rows beyond one piece are copied piece by piece into
 // the same buffer.
-template <int CPT>
+template <int CPT, bool RESID>
 __global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
     beam_token_bulk_kernel(const BeamArgs a, const int rows_per_piece) {
     extern __shared__ __align__(128) uint8_t rows_smem[];
     __shared__ uint64_t bar;
     __shared__ float red[32];
+    __shared__ float red2[32];
     __shared__ float wsm[32];
     const int NT = blockDim.x;
     const int tid = threadIdx.x;
@@ -175,6 +237,10 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
         fence_mbar_init();
     }
     pdl_wait();
+    if constexpr (RESID) {
+        // the residual row is read in the epilogue: start bringing it into L2
+        if (tid == (NT > 32 ? 32 : 0)) bulk_prefetch_l2(a.residual + t * H, row_bytes);
+    }
     if (tid < K) wsm[tid] = __ldg(a.weights + t * K + tid);
     __syncthreads();
 
@@ -228,7 +294,11 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
         for (int i = 0; i < nw; ++i) tot += red[i];
         rs = inv_rms(tot, H, a.post_eps);
     }
-    if (ok) beam_store<CPT>(acc, a, norm, rs, a.out + t * H, tid, NT);
+    if constexpr (RESID) {
+        residual_epilogue<CPT>(acc, a, norm, rs, t, tid, NT, red2, ok);
+    } else {
+        if (ok) beam_store<CPT>(acc, a, norm, rs, a.out + t * H, tid, NT);
+    }
     pdl_trigger();
 }
 
@@ -273,11 +343,11 @@ __global__ void wait_timeout_selftest_kernel(unsigned *status, uint64_t timeout_
 
 cudaError_t prepare_beam_kernels(int smem_per_sm) {
     const int budget = beam_bulk_budget(smem_per_sm);
-    cudaError_t e = cudaFuncSetAttribute(beam_token_bulk_kernel<1>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(beam_token_bulk_kernel<2>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, budget);
+    const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, false>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, false>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, true>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, true>, attr, budget);
     return e;
 }
 
@@ -292,13 +362,18 @@ cudaError_t launch_beam_token_cta(const BeamArgs &a, cudaStream_t s) {
     }
 }
 
-cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, cudaStream_t s) {
+cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, bool residual, cudaStream_t s) {
     const int cpt = beam_bulk_cpt(a.hidden);
     const int rows = beam_bulk_rows(smem_per_sm, a.top_k, a.hidden);
     const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;
     const dim3 grid(static_cast<unsigned>(a.live)), block(a.hidden / 8 / cpt);
-    if (cpt == 2) return launch_ex(beam_token_bulk_kernel<2>, grid, block, bytes, s, 1, a.programmatic, a, rows);
-    return launch_ex(beam_token_bulk_kernel<1>, grid, block, bytes, s, 1, a.programmatic, a, rows);
+    const bool p = a.programmatic;
+    if (residual) {
+        if (cpt == 2) return launch_ex(beam_token_bulk_kernel<2, true>, grid, block, bytes, s, 1, p, a, rows);
+        return launch_ex(beam_token_bulk_kernel<1, true>, grid, block, bytes, s, 1, p, a, rows);
+    }
+    if (cpt == 2) return launch_ex(beam_token_bulk_kernel<2, false>, grid, block, bytes, s, 1, p, a, rows);
+    return launch_ex(beam_token_bulk_kernel<1, false>, grid, block, bytes, s, 1, p, a, rows);
 }
 
 cudaError_t launch_wait_timeout_selftest(unsigned *status, uint64_t timeout_ns, cudaStream_t s) {

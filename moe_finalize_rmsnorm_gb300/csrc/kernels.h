@@ -39,7 +39,7 @@ struct TpArgs {
 struct BeamArgs {
     const uint16_t *x;           // BF16 [capacity, K, H]
     const float *weights;        // FP32 [>= live, K]
-    uint16_t *out;               // BF16 [live, H]
+    uint16_t *out;               // BF16 [live, H] (the hidden output with a residual)
     const uint16_t *post_weight; // BF16 [H] or nullptr
     int64_t live;
     int top_k;
@@ -50,6 +50,14 @@ struct BeamArgs {
     unsigned *status;
     uint64_t timeout_ns;
     bool programmatic;
+    // residual step (beam_moe_finalize_norm_residual_norm); unused otherwise
+    const uint16_t *residual;    // BF16 [live, H]
+    const uint16_t *next_weight; // BF16 [H] or nullptr
+    uint16_t *normalized;        // BF16 [live, H] when has_next
+    float next_eps;
+    int has_next;
+    float scale_x;
+    float scale_residual;
 };
 
 // Per-device one-time set-up (kernel attributes).  `smem_optin` is the
@@ -66,7 +74,9 @@ cudaError_t launch_tp_bulk(const TpArgs &a, int weight_kind, cudaStream_t s);
 cudaError_t launch_tp_generic(const TpArgs &a, int weight_kind, int smem_per_sm, cudaStream_t s);
 
 cudaError_t launch_beam_token_cta(const BeamArgs &a, cudaStream_t s);
-cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, cudaStream_t s);
+// `residual`: finalize, then the residual-add and next norm of
+// beam_moe_finalize_norm_residual_norm.
+cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, bool residual, cudaStream_t s);
 
 cudaError_t launch_wait_timeout_selftest(unsigned *status, uint64_t timeout_ns, cudaStream_t s);
 

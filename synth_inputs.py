@@ -256,3 +256,9 @@ def algorithmic_bytes_tp(tokens: int, hidden: int = 4096, top_k: int = 8,
 def algorithmic_bytes_beam(live_tokens: int, hidden: int, top_k: int) -> int:
     """K*H*2 read + H*2 written + K*4 weight bytes, per live token."""
     return live_tokens * (top_k * hidden * 2 + hidden * 2 + top_k * 4)
+
+
+def algorithmic_bytes_beam_residual(tokens: int, hidden: int, top_k: int, next_norm: bool) -> int:
+    """Beam bytes plus the residual read, the hidden write and (with the next
+    norm) the normalized write, per token."""
+    return tokens * (top_k * hidden * 2 + top_k * 4 + hidden * 2 * (3 if next_norm else 2))

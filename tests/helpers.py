@@ -33,9 +33,17 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return f64_to_bf16_bits(np.asarray(x, dtype=np.float32).astype(np.float64))
 
 
+def bf16_ulp(bits: np.ndarray) -> np.ndarray:
+    """Spacing of BF16 values at each element (16 fewer significand bits than float32)."""
+    f = np.abs(bf16_bits_to_f64(bits)).astype(np.float32)
+    return np.spacing(f).astype(np.float64) * 65536.0
+
+
 def compare_bf16(got: np.ndarray, ref: np.ndarray, *, rel: float = REL_TOL, abs_: float = ABS_TOL,
-                 min_exact: float = MIN_EXACT) -> dict:
-    """Element-wise check of BF16 bit arrays; returns stats, raises AssertionError."""
+                 min_exact: float = MIN_EXACT, extra: np.ndarray | None = None) -> dict:
+    """Element-wise check of BF16 bit arrays; returns stats, raises AssertionError.
+    ``extra`` (same shape) widens the bound per element where an intermediate
+    BF16 rounding propagates (the caller derives it)."""
     got = np.asarray(got, dtype=np.uint16)
     ref = np.asarray(ref, dtype=np.uint16)
     assert got.shape == ref.shape, (got.shape, ref.shape)
@@ -53,6 +61,8 @@ def compare_bf16(got: np.ndarray, ref: np.ndarray, *, rel: float = REL_TOL, abs_
     with np.errstate(invalid="ignore"):
         err = np.abs(g - r)
         bound = rel * np.abs(r) + abs_
+        if extra is not None:
+            bound = bound + extra
         bad = fin & ~(err <= bound)
     n = got.size
     stats = dict(n=n, exact_frac=float(exact.sum()) / max(n, 1),

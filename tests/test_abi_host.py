@@ -167,3 +167,26 @@ def test_ctypes_signatures_match_header_arity():
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(params) == len(args), (name, len(params), len(args))
     assert ctypes.sizeof(ctypes.c_void_p) == 8
+
+
+def resid(lib, x=A, cap=10, w=A, wrows=10, r=A, T=5, K=8, H=7168, pw=A, pn=1, nw=A, nn=1,
+          hid=A, nrm=A):
+    return lib.beam_moe_finalize_norm_residual_norm(x, cap, w, wrows, r, T, K, H, 2.5, pw, 1e-6,
+                                                    pn, nw, 1e-6, nn, 1.0, 1.0, hid, nrm, None)
+
+
+def test_residual_norm_validation(lib):
+    assert resid(lib, K=33) == UNSUP
+    assert resid(lib, H=300) == UNSUP
+    assert resid(lib, T=11) == SHAPE               # more tokens than capacity
+    assert resid(lib, wrows=4) == SHAPE
+    assert resid(lib, pn=0) == INVALID             # post_weight without its eps
+    assert resid(lib, nn=0) == INVALID             # next_weight without its eps
+    assert resid(lib, nw=None, nn=0) == INVALID    # normalized output without the next norm
+    assert resid(lib, r=None) == NULL
+    assert resid(lib, hid=None) == NULL
+    assert resid(lib, nrm=None) == NULL            # next norm without its output
+    assert resid(lib, r=MIS) == ALIGN
+    assert resid(lib, nrm=MIS) == ALIGN
+    assert resid(lib, nw=MIS) == ALIGN
+    assert resid(lib, x=None, w=None, r=None, hid=None, nrm=None, T=0) == OK

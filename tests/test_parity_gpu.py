@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 import synth_inputs as si
-from helpers import bf16_bits_to_f64, compare_bf16
+from helpers import bf16_bits_to_f64, bf16_ulp, compare_bf16
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -478,3 +478,98 @@ def test_graph_replay_with_new_inputs(cuda_lib, variant):
         graph.replay()
         torch.cuda.synchronize()
         compare_bf16(host_bits(out), oracle_tp(c))
+
+
+
+# ---------------------------------------------------------------------------
+# beam_moe_finalize_norm_residual_norm (residual step: a reading of the pages)
+
+def residual_bounds(case, h_ref, n_ref, *, post, scales, next_eps, next_weight):
+    """Widened bounds for the residual op.  With the Beam post-norm on, the
+    finalized value f = BF16(v * rs * post_weight) comes from an FP32 norm on
+    the GPU and a float64 one in the oracle, so f may land one BF16 ulp apart
+    (about 1e-5 of elements); hidden = BF16(s0 f + s1 r) then differs by up to
+    |s0| ulp(f) on top of its own rounding, which can be many ulps of hidden
+    where s0 f and s1 r cancel.  The next norm scales that by rn * next_weight.
+    Without the post-norm f is bit-exact and no widening applies."""
+    if not post:
+        return None, None
+    T = h_ref.shape[0]
+    f_ref = oracle.beam_moe_finalize(case.expert_outputs, case.weights, T,
+                                     routed_scale=case.routed_scale,
+                                     post_weight=case.post_weight, post_eps=1e-6)
+    s0 = 1.0 if scales is None else scales[0]
+    eh = abs(s0) * bf16_ulp(f_ref)
+    if n_ref is None:
+        return eh, None
+    hv = bf16_bits_to_f64(h_ref)
+    rn = 1.0 / np.sqrt((hv * hv).mean(axis=1, keepdims=True) + next_eps)
+    g = np.abs(bf16_bits_to_f64(next_weight)) if next_weight is not None else 1.0
+    return eh, (eh + bf16_ulp(h_ref)) * rn * g
+
+
+def run_residual(mf, case, residual_bits, *, post, nxt, scales, inplace=False, tokens=None):
+    cap, K, H = case.expert_outputs.shape
+    x = dev_bf16(case.expert_outputs.reshape(cap * K, H))
+    w = torch.from_numpy(case.weights).cuda()
+    r = dev_bf16(residual_bits)
+    pw = dev_bf16(case.post_weight) if (post and case.post_weight is not None) else None
+    nw = dev_bf16(case.post_weight[::-1].copy()) if nxt == "weighted" else None
+    hid_out = r if inplace else None
+    h, n = mf.beam_moe_finalize_norm_residual_norm(
+        x, w, r, pw, 1e-6 if post else None, nw, 1e-5 if nxt else None, scales,
+        case.routed_scale, hidden=hid_out)
+    torch.cuda.synchronize()
+    if inplace:
+        assert h.data_ptr() == r.data_ptr()
+    return host_bits(h), (host_bits(n) if n is not None else None), nw
+
+
+@pytest.mark.parametrize("post", [True, False])
+@pytest.mark.parametrize("nxt", [None, "weighted", "plain"])
+@pytest.mark.parametrize("scales", [None, (0.5, 2.0)])
+def test_residual_norm_matches_oracle(cuda_lib, post, nxt, scales):
+    cap, K, H, T = 300, 8, 7168, 290
+    case = si.beam_case("resid", cap, K, H, T, routed_scale=2.5, seed=60, poison_dead_rows=True)
+    res = si.normal_bf16((T, H), 1.0, 61, 1)
+    h, n, _ = run_residual(cuda_lib, case, res, post=post, nxt=nxt, scales=scales)
+    rh, rn = oracle.beam_moe_finalize_norm_residual_norm(
+        case.expert_outputs, case.weights, res, routed_scale=2.5,
+        post_weight=case.post_weight if post else None, post_eps=1e-6 if post else None,
+        next_weight=case.post_weight[::-1].copy() if nxt == "weighted" else None,
+        next_eps=1e-5 if nxt else None, scales=scales)
+    eh, en = residual_bounds(case, rh, rn, post=post, scales=scales, next_eps=1e-5,
+                             next_weight=case.post_weight[::-1].copy() if nxt == "weighted" else None)
+    compare_bf16(h, rh, extra=eh)
+    if nxt:
+        compare_bf16(n, rn, extra=en)
+    else:
+        assert n is None and rn is None
+    if not post:
+        assert np.array_equal(h, rh)   # no norm on the way to hidden: bit-exact
+
+
+@pytest.mark.parametrize("K,H", [(1, 256), (32, 8192), (3, 7936), (16, 2048)])
+def test_residual_norm_shapes_and_in_place(cuda_lib, K, H):
+    cap, T = 40, 37
+    case = si.beam_case("resid_shapes", cap, K, H, T, routed_scale=1.5, seed=K + H)
+    res = si.normal_bf16((T, H), 2.0, 62, 1)
+    h, n, nw = run_residual(cuda_lib, case, res, post=True, nxt="weighted", scales=(1.25, -0.75),
+                            inplace=True)
+    rh, rn = oracle.beam_moe_finalize_norm_residual_norm(
+        case.expert_outputs, case.weights, res, routed_scale=1.5, post_weight=case.post_weight,
+        post_eps=1e-6, next_weight=case.post_weight[::-1].copy(), next_eps=1e-5,
+        scales=(1.25, -0.75))
+    eh, en = residual_bounds(case, rh, rn, post=True, scales=(1.25, -0.75), next_eps=1e-5,
+                             next_weight=case.post_weight[::-1].copy())
+    compare_bf16(h, rh, extra=eh)
+    compare_bf16(n, rn, extra=en)
+
+
+def test_residual_norm_zero_tokens(cuda_lib):
+    case = si.beam_case("resid0", 4, 2, 256, 4, seed=63)
+    x = dev_bf16(case.expert_outputs.reshape(8, 256))
+    r = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    h, n = cuda_lib.beam_moe_finalize_norm_residual_norm(
+        x, torch.from_numpy(case.weights).cuda(), r, None, None, None, 1e-6, None)
+    assert h.shape == (0, 256) and n.shape == (0, 256)
