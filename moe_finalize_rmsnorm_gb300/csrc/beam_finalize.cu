@@ -48,29 +48,36 @@ __device__ __forceinline__ float sum_squares(const float (&v)[CPT][8]) {
     return ss;
 }
 
+// post_weight chunks of this thread (BF16 packed), loaded early so the
+// epilogue does not wait on them; ones when absent.
+template <int CPT>
+__device__ __forceinline__ void load_post_weight(const BeamArgs &a, int chunk0, int stride,
+                                                 uint4 (&pw)[CPT]) {
+#pragma unroll
+    for (int c = 0; c < CPT; ++c)
+        pw[c] = a.post_weight ? __ldg(reinterpret_cast<const uint4 *>(a.post_weight) + chunk0 +
+                                      c * stride)
+                              : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+}
+
 // Store v (no norm) or v * rs * post_weight, rounded to BF16.
 template <int CPT>
-__device__ __forceinline__ void beam_store(const float (&v)[CPT][8], const BeamArgs &a, bool norm,
-                                           float rs, uint16_t *out_row, int chunk0, int stride) {
+__device__ __forceinline__ void beam_store(const float (&v)[CPT][8], const uint4 (&pwq)[CPT],
+                                           bool norm, float rs, uint16_t *out_row, int chunk0,
+                                           int stride) {
 #pragma unroll
     for (int c = 0; c < CPT; ++c) {
-        const int chunk = chunk0 + c * stride;
         float y[8];
         if (norm) {
             float pw[8];
-            if (a.post_weight) {
-                unpack8(__ldg(reinterpret_cast<const uint4 *>(a.post_weight) + chunk), pw);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) pw[j] = 1.f;
-            }
+            unpack8(pwq[c], pw);
 #pragma unroll
             for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(__fmul_rn(v[c][j], rs), pw[j]);
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) y[j] = v[c][j];  // already BF16 values: exact
         }
-        st_cs_16(out_row + static_cast<int64_t>(chunk) * kChunkElems, pack8_rn(y));
+        st_cs_16(out_row + static_cast<int64_t>(chunk0 + c * stride) * kChunkElems, pack8_rn(y));
     }
 }
 
@@ -131,6 +138,8 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
 
     round_scale_round<CPT>(acc, a.routed_scale);
     const bool norm = a.has_norm != 0;
+    uint4 pwq[CPT];
+    load_post_weight<CPT>(a, tid, NT, pwq);
     float rs = 1.f;
     if (norm) {
         const float ss = warp_sum(sum_squares<CPT>(acc));
@@ -141,7 +150,7 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
         for (int i = 0; i < nw; ++i) tot += red[i];
         rs = inv_rms(tot, H, a.post_eps);
     }
-    beam_store<CPT>(acc, a, norm, rs, a.out + t * H, tid, NT);
+    beam_store<CPT>(acc, pwq, norm, rs, a.out + t * H, tid, NT);
     pdl_trigger();
 }
 
@@ -152,9 +161,9 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
 // reads the residual chunks it then overwrites, so hidden may be written into
 // the residual buffer itself.
 template <int CPT>
-__device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const BeamArgs &a, bool norm,
-                                                  float rs, int64_t t, int tid, int NT, float *red,
-                                                  bool ok) {
+__device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const uint4 (&pwq)[CPT],
+                                                  const BeamArgs &a, bool norm, float rs,
+                                                  int64_t t, int tid, int NT, float *red, bool ok) {
     const int H = a.hidden;
     const uint16_t *res_row = a.residual + t * H;
     uint16_t *hid_row = a.out + t * H;
@@ -165,12 +174,7 @@ __device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const Beam
         float r[8];
         unpack8(ld_nc_na_16(res_row + static_cast<int64_t>(chunk) * kChunkElems), r);
         float pw[8];
-        if (norm && a.post_weight) {
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(a.post_weight) + chunk), pw);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) pw[j] = 1.f;
-        }
+        unpack8(pwq[c], pw);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const float f = norm ? round_bf16(__fmul_rn(__fmul_rn(v[c][j], rs), pw[j])) : v[c][j];
@@ -209,17 +213,17 @@ __device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const Beam
 // ---------------------------------------------------------------------------
 // one CTA per live token, the token's rows staged in shared memory
 
-// A token's K rows are contiguous, so thread 0 moves them with one bulk copy
-// per piece (as many whole rows as fit half an SM's shared memory: all 8 rows,
-// 114,688 B, at H = 7168), completing on one mbarrier.  Data in flight holds
+// Thread 0 moves the token's rows with one bulk copy per row into a buffer of
+// as many whole rows as fit half an SM's shared memory (all 8 rows, 114,688 B,
+// at H = 7168), each row completing on its own mbarrier.  Data in flight holds
 // no registers, and two CTAs per SM keep two tokens' blocks in flight while
 // one of them reduces.  Rows beyond one piece are copied piece by piece into
 // the same buffer.
 template <int CPT, bool RESID>
-__global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
+__global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
     beam_token_bulk_kernel(const BeamArgs a, const int rows_per_piece) {
     extern __shared__ __align__(128) uint8_t rows_smem[];
-    __shared__ uint64_t bar;
+    __shared__ uint64_t bars[32];
     __shared__ float red[32];
     __shared__ float red2[32];
     __shared__ float wsm[32];
@@ -229,11 +233,12 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
     const int K = a.top_k, H = a.hidden;
     const uint32_t row_bytes = static_cast<uint32_t>(H) * 2;
     const uint32_t base = smem_u32(rows_smem);
-    const uint32_t bar_addr = smem_u32(&bar);
     const uint16_t *xt = a.x + t * K * static_cast<int64_t>(H);
 
+    // one mbarrier per buffered row: the reduction starts on a row as soon as
+    // it lands
     if (tid == 0) {
-        mbar_init(bar_addr, 1);
+        for (int r = 0; r < rows_per_piece; ++r) mbar_init(smem_u32(&bars[r]), 1);
         fence_mbar_init();
     }
     pdl_wait();
@@ -242,6 +247,8 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
         if (tid == (NT > 32 ? 32 : 0)) bulk_prefetch_l2(a.residual + t * H, row_bytes);
     }
     if (tid < K) wsm[tid] = __ldg(a.weights + t * K + tid);
+    uint4 pwq[CPT];  // post_weight, fetched while the rows are in flight
+    load_post_weight<CPT>(a, tid, NT, pwq);
     __syncthreads();
 
     float acc[CPT][8];
@@ -256,16 +263,21 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
         const int n = K - k0 < rows_per_piece ? K - k0 : rows_per_piece;
         if (tid == 0) {
             if (k0 > 0) fence_proxy_async_smem();  // earlier reads of the buffer come first
-            mbar_arrive_expect_tx(bar_addr, n * row_bytes);
-            bulk_copy_g2s_hint(base, xt + static_cast<int64_t>(k0) * H, n * row_bytes, bar_addr,
-                               policy_evict_first());
-        }
-        if (!mbar_wait(bar_addr, phase, a.timeout_ns)) {
-            atomicOr(a.status, kStatusWaitTimeout);
-            ok = false;
-            (void)mbar_wait(bar_addr, phase, a.timeout_ns);  // let the copy land before exit
+            const uint64_t policy = policy_evict_first();
+            for (int r = 0; r < n; ++r) {
+                const uint32_t b = smem_u32(&bars[r]);
+                mbar_arrive_expect_tx(b, row_bytes);
+                bulk_copy_g2s_hint(base + r * row_bytes, xt + static_cast<int64_t>(k0 + r) * H,
+                                   row_bytes, b, policy);
+            }
         }
         for (int r = 0; r < n; ++r) {
+            const uint32_t b = smem_u32(&bars[r]);
+            if (!mbar_wait(b, phase, a.timeout_ns)) {
+                atomicOr(a.status, kStatusWaitTimeout);
+                ok = false;
+                (void)mbar_wait(b, phase, a.timeout_ns);  // let the copy land before exit
+            }
             const float w = wsm[k0 + r];
             const uint32_t row = base + static_cast<uint32_t>(r) * row_bytes;
             uint4 q[CPT];
@@ -295,9 +307,9 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), 1)
         rs = inv_rms(tot, H, a.post_eps);
     }
     if constexpr (RESID) {
-        residual_epilogue<CPT>(acc, a, norm, rs, t, tid, NT, red2, ok);
+        residual_epilogue<CPT>(acc, pwq, a, norm, rs, t, tid, NT, red2, ok);
     } else {
-        if (ok) beam_store<CPT>(acc, a, norm, rs, a.out + t * H, tid, NT);
+        if (ok) beam_store<CPT>(acc, pwq, norm, rs, a.out + t * H, tid, NT);
     }
     pdl_trigger();
 }
@@ -318,9 +330,9 @@ int beam_bulk_cpt(int hidden) {
 }
 
 // Shared memory one staged CTA may use so that two fit on an SM (each CTA
-// also takes 1 KB reserved by the system and a few hundred bytes of static
-// shared memory).
-int beam_bulk_budget(int smem_per_sm) { return smem_per_sm / 2 - 1024 - 512; }
+// also takes 1 KB reserved by the system and up to 1 KB of static shared
+// memory: barriers, reduction and weight arrays).
+int beam_bulk_budget(int smem_per_sm) { return smem_per_sm / 2 - 1024 - 1024; }
 
 int beam_bulk_rows(int smem_per_sm, int top_k, int hidden) {
     const int rows = beam_bulk_budget(smem_per_sm) / (hidden * 2);

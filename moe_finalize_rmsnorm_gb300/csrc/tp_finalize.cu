@@ -24,7 +24,7 @@
 //                        memory, so a token's 64 KB gather spreads over C SMs.
 //   tp_token_bulk_kernel one CTA per token; thread 0 stages the token's valid
 //                        rows in shared memory with 1-D bulk copies
-//                        (cp.async.bulk) completing on one mbarrier, so no
+//                        (cp.async.bulk), one mbarrier per row, so no
 //                        registers are held by data in flight and three
 //                        CTAs (192 KB of rows) fit per SM.
 //   tp_generic_bulk_kernel  any (hidden, top-k) in range: the staged design
@@ -264,13 +264,12 @@ __global__ void __launch_bounds__(kBulkThreads)
     tp_token_bulk_kernel(const TpArgs a) {
     constexpr int NT = kBulkThreads, NW = NT / 32, CPT = kBulkCPT;
     extern __shared__ __align__(128) uint8_t rows_smem[];
-    __shared__ uint64_t bar;
+    __shared__ uint64_t bars[8];
     __shared__ float red[NW];
 
     const int64_t t = blockIdx.x;
     const int tid = threadIdx.x;
     const uint32_t rows_base = smem_u32(rows_smem);
-    const uint32_t bar_addr = smem_u32(&bar);
 
     pdl_wait();
     int idx[8];
@@ -280,37 +279,42 @@ __global__ void __launch_bounds__(kBulkThreads)
 #pragma unroll
     for (int k = 0; k < 8; ++k) mask |= (slot_valid(idx[k], a.rows) ? 1u : 0u) << k;
 
+    // one mbarrier per row: the reduction starts on a row as soon as it lands
     if (tid == 0) {
-        mbar_init(bar_addr, 1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mbar_init(smem_u32(&bars[k]), 1);
         fence_mbar_init();
         const uint64_t policy = policy_evict_first();
-        mbar_arrive_expect_tx(bar_addr, static_cast<uint32_t>(__popc(mask)) * kTpRowBytes);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            if ((mask >> k) & 1u)
+            if ((mask >> k) & 1u) {
+                const uint32_t b = smem_u32(&bars[k]);
+                mbar_arrive_expect_tx(b, kTpRowBytes);
                 bulk_copy_g2s_hint(rows_base + k * kTpRowBytes,
-                                   a.gemm2 + static_cast<int64_t>(idx[k]) * a.ld, kTpRowBytes,
-                                   bar_addr, policy);
+                                   a.gemm2 + static_cast<int64_t>(idx[k]) * a.ld, kTpRowBytes, b,
+                                   policy);
+            }
     }
     float g[CPT][8];
 #pragma unroll
     for (int c = 0; c < CPT; ++c) load_gain(a, tid + c * NT, g[c]);
-    __syncthreads();  // the barrier is initialised before anyone waits on it
-
-    bool ok = mbar_wait(bar_addr, 0u, a.timeout_ns);
-    if (!ok) {
-        atomicOr(a.status, kStatusWaitTimeout);
-        ok = mbar_wait(bar_addr, 0u, a.timeout_ns);  // let copies in flight land before exit
-    }
+    __syncthreads();  // the barriers are initialised before anyone waits on them
 
     float acc[CPT][8];
 #pragma unroll
     for (int c = 0; c < CPT; ++c)
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc[c][j] = 0.f;
+    bool ok = true;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         if (!((mask >> k) & 1u)) continue;
+        const uint32_t b = smem_u32(&bars[k]);
+        if (!mbar_wait(b, 0u, a.timeout_ns)) {
+            atomicOr(a.status, kStatusWaitTimeout);
+            ok = false;
+            (void)mbar_wait(b, 0u, a.timeout_ns);  // let the copy land before exit
+        }
         uint4 q[CPT];
 #pragma unroll
         for (int c = 0; c < CPT; ++c) q[c] = lds_16(rows_base + k * kTpRowBytes + (tid + c * NT) * kChunkBytes);
