@@ -154,25 +154,28 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
     pdl_trigger();
 }
 
-// Residual step of beam_moe_finalize_norm_residual_norm: the finalized value
+// Residual step of beam_moe_finalize_norm_residual_norm (residual and
+// next_weight chunks are loaded by the caller while the rows are in flight):
+// the finalized value
 // f = BF16(v * rs * post_weight) (or v), then hidden = BF16(s0 f + s1 residual)
 // in FP32 (one product, one FMA), stored; with the next norm, normalized =
 // BF16(hidden * rsqrt(mean(hidden^2) + next_eps) * next_weight).  Each thread
-// reads the residual chunks it then overwrites, so hidden may be written into
+// reads the residual chunks it later overwrites, so hidden may be written into
 // the residual buffer itself.
 template <int CPT>
 __device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const uint4 (&pwq)[CPT],
-                                                  const BeamArgs &a, bool norm, float rs,
-                                                  int64_t t, int tid, int NT, float *red, bool ok) {
+                                                  const uint4 (&resq)[CPT],
+                                                  const uint4 (&nwq)[CPT], const BeamArgs &a,
+                                                  bool norm, float rs, int64_t t, int tid, int NT,
+                                                  float *red, bool ok) {
     const int H = a.hidden;
-    const uint16_t *res_row = a.residual + t * H;
     uint16_t *hid_row = a.out + t * H;
     float ss = 0.f;
 #pragma unroll
     for (int c = 0; c < CPT; ++c) {
         const int chunk = tid + c * NT;
         float r[8];
-        unpack8(ld_nc_na_16(res_row + static_cast<int64_t>(chunk) * kChunkElems), r);
+        unpack8(resq[c], r);
         float pw[8];
         unpack8(pwq[c], pw);
 #pragma unroll
@@ -197,12 +200,7 @@ __device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const uint
     for (int c = 0; c < CPT; ++c) {
         const int chunk = tid + c * NT;
         float g[8];
-        if (a.next_weight) {
-            unpack8(__ldg(reinterpret_cast<const uint4 *>(a.next_weight) + chunk), g);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) g[j] = 1.f;
-        }
+        unpack8(nwq[c], g);
         float y[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) y[j] = __fmul_rn(__fmul_rn(v[c][j], rn), g[j]);
@@ -242,13 +240,20 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
         fence_mbar_init();
     }
     pdl_wait();
-    if constexpr (RESID) {
-        // the residual row is read in the epilogue: start bringing it into L2
-        if (tid == (NT > 32 ? 32 : 0)) bulk_prefetch_l2(a.residual + t * H, row_bytes);
-    }
     if (tid < K) wsm[tid] = __ldg(a.weights + t * K + tid);
     uint4 pwq[CPT];  // post_weight, fetched while the rows are in flight
     load_post_weight<CPT>(a, tid, NT, pwq);
+    uint4 resq[CPT], nwq[CPT];  // residual step: residual and next_weight chunks, same
+    if constexpr (RESID) {
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+            const int chunk = tid + c * NT;
+            resq[c] = ld_nc_na_16(a.residual + t * H + static_cast<int64_t>(chunk) * kChunkElems);
+            nwq[c] = a.next_weight
+                         ? __ldg(reinterpret_cast<const uint4 *>(a.next_weight) + chunk)
+                         : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        }
+    }
     __syncthreads();
 
     float acc[CPT][8];
@@ -307,7 +312,7 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
         rs = inv_rms(tot, H, a.post_eps);
     }
     if constexpr (RESID) {
-        residual_epilogue<CPT>(acc, pwq, a, norm, rs, t, tid, NT, red2, ok);
+        residual_epilogue<CPT>(acc, pwq, resq, nwq, a, norm, rs, t, tid, NT, red2, ok);
     } else {
         if (ok) beam_store<CPT>(acc, pwq, norm, rs, a.out + t * H, tid, NT);
     }
