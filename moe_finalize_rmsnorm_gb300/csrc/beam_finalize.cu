@@ -217,11 +217,13 @@ __device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const uint
 // no registers, and two CTAs per SM keep two tokens' blocks in flight while
 // one of them reduces.  Rows beyond one piece are copied piece by piece into
 // the same buffer.
-template <int CPT, bool RESID>
+// PER_ROW: one mbarrier per buffered row (rows of 4 KB and more); otherwise
+// one copy and one mbarrier per piece (small rows).
+template <int CPT, bool RESID, bool PER_ROW>
 __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
     beam_token_bulk_kernel(const BeamArgs a, const int rows_per_piece) {
     extern __shared__ __align__(128) uint8_t rows_smem[];
-    __shared__ uint64_t bars[32];
+    __shared__ uint64_t bars[PER_ROW ? 32 : 1];
     __shared__ float red[32];
     __shared__ float red2[32];
     __shared__ float wsm[32];
@@ -236,7 +238,7 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
     // one mbarrier per buffered row: the reduction starts on a row as soon as
     // it lands
     if (tid == 0) {
-        for (int r = 0; r < rows_per_piece; ++r) mbar_init(smem_u32(&bars[r]), 1);
+        for (int r = 0; r < (PER_ROW ? rows_per_piece : 1); ++r) mbar_init(smem_u32(&bars[r]), 1);
         fence_mbar_init();
     }
     pdl_wait();
@@ -269,19 +271,28 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
         if (tid == 0) {
             if (k0 > 0) fence_proxy_async_smem();  // earlier reads of the buffer come first
             const uint64_t policy = policy_evict_first();
-            for (int r = 0; r < n; ++r) {
-                const uint32_t b = smem_u32(&bars[r]);
-                mbar_arrive_expect_tx(b, row_bytes);
-                bulk_copy_g2s_hint(base + r * row_bytes, xt + static_cast<int64_t>(k0 + r) * H,
-                                   row_bytes, b, policy);
+            if (PER_ROW) {
+                for (int r = 0; r < n; ++r) {
+                    const uint32_t b = smem_u32(&bars[r]);
+                    mbar_arrive_expect_tx(b, row_bytes);
+                    bulk_copy_g2s_hint(base + r * row_bytes, xt + static_cast<int64_t>(k0 + r) * H,
+                                       row_bytes, b, policy);
+                }
+            } else {  // the piece's rows are contiguous: one copy
+                const uint32_t b = smem_u32(&bars[0]);
+                mbar_arrive_expect_tx(b, n * row_bytes);
+                bulk_copy_g2s_hint(base, xt + static_cast<int64_t>(k0) * H, n * row_bytes, b,
+                                   policy);
             }
         }
         for (int r = 0; r < n; ++r) {
-            const uint32_t b = smem_u32(&bars[r]);
-            if (!mbar_wait(b, phase, a.timeout_ns)) {
-                atomicOr(a.status, kStatusWaitTimeout);
-                ok = false;
-                (void)mbar_wait(b, phase, a.timeout_ns);  // let the copy land before exit
+            if (PER_ROW || r == 0) {
+                const uint32_t b = smem_u32(&bars[PER_ROW ? r : 0]);
+                if (!mbar_wait(b, phase, a.timeout_ns)) {
+                    atomicOr(a.status, kStatusWaitTimeout);
+                    ok = false;
+                    (void)mbar_wait(b, phase, a.timeout_ns);  // let the copy land before exit
+                }
             }
             const float w = wsm[k0 + r];
             const uint32_t row = base + static_cast<uint32_t>(r) * row_bytes;
@@ -361,10 +372,13 @@ __global__ void wait_timeout_selftest_kernel(unsigned *status, uint64_t timeout_
 cudaError_t prepare_beam_kernels(int smem_per_sm) {
     const int budget = beam_bulk_budget(smem_per_sm);
     const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    cudaError_t e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, false>, attr, budget);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, false>, attr, budget);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, true>, attr, budget);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, true>, attr, budget);
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, false, false>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, true, false>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, false, true>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, true, true>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, false, true>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, true, true>, attr, budget);
     return e;
 }
 
@@ -385,12 +399,17 @@ cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, bool residual, 
     const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;
     const dim3 grid(static_cast<unsigned>(a.live)), block(a.hidden / 8 / cpt);
     const bool p = a.programmatic;
-    if (residual) {
-        if (cpt == 2) return launch_ex(beam_token_bulk_kernel<2, true>, grid, block, bytes, s, 1, p, a, rows);
-        return launch_ex(beam_token_bulk_kernel<1, true>, grid, block, bytes, s, 1, p, a, rows);
+    // CPT 2 implies hidden >= 4096 (rows of 8 KB and more): per-row barriers
+    if (cpt == 2) {
+        if (residual) return launch_ex(beam_token_bulk_kernel<2, true, true>, grid, block, bytes, s, 1, p, a, rows);
+        return launch_ex(beam_token_bulk_kernel<2, false, true>, grid, block, bytes, s, 1, p, a, rows);
     }
-    if (cpt == 2) return launch_ex(beam_token_bulk_kernel<2, false>, grid, block, bytes, s, 1, p, a, rows);
-    return launch_ex(beam_token_bulk_kernel<1, false>, grid, block, bytes, s, 1, p, a, rows);
+    if (a.hidden >= 2048) {
+        if (residual) return launch_ex(beam_token_bulk_kernel<1, true, true>, grid, block, bytes, s, 1, p, a, rows);
+        return launch_ex(beam_token_bulk_kernel<1, false, true>, grid, block, bytes, s, 1, p, a, rows);
+    }
+    if (residual) return launch_ex(beam_token_bulk_kernel<1, true, false>, grid, block, bytes, s, 1, p, a, rows);
+    return launch_ex(beam_token_bulk_kernel<1, false, false>, grid, block, bytes, s, 1, p, a, rows);
 }
 
 cudaError_t launch_wait_timeout_selftest(unsigned *status, uint64_t timeout_ns, cudaStream_t s) {

@@ -367,11 +367,14 @@ constexpr int generic_max_threads() { return CPT == 2 ? 512 : 1024; }
 template <int CPT>
 constexpr int generic_min_blocks() { return CPT == 2 ? 2 : 1; }
 
-template <int CPT, int WK>
+// PER_ROW: one mbarrier per buffered row, so the reduction starts on a row as
+// soon as it lands (rows of 4 KB and more); otherwise one per piece (small
+// rows, where a wait per row costs more than it overlaps).
+template <int CPT, int WK, bool PER_ROW>
 __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks<CPT>())
     tp_generic_bulk_kernel(const TpArgs a, const int rows_per_piece) {
     extern __shared__ __align__(128) uint8_t rows_smem[];
-    __shared__ uint64_t bar;
+    __shared__ uint64_t bars[PER_ROW ? 32 : 1];
     __shared__ float red[32];
     __shared__ float w_s[32];
     __shared__ int idx_s[32];
@@ -384,7 +387,7 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
     const int H = a.hidden, K = a.top_k;
     const uint32_t row_bytes = static_cast<uint32_t>(H) * 2;
     const uint32_t base = smem_u32(rows_smem);
-    const uint32_t bar_addr = smem_u32(&bar);
+    const uint32_t bar_addr = smem_u32(&bars[0]);
 
     pdl_wait();
     if (tid < 32) {
@@ -397,11 +400,9 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
         idx_s[tid] = i;
         w_s[tid] = w;
         if (valid) order_s[__popc(mask & ((1u << tid) - 1u))] = tid;
-        if (tid == 0) {
-            nvalid_s = __popc(mask);
-            mbar_init(bar_addr, 1);
-            fence_mbar_init();
-        }
+        if (PER_ROW ? tid < rows_per_piece : tid == 0) mbar_init(smem_u32(&bars[tid]), 1);
+        if (tid == 0) nvalid_s = __popc(mask);
+        fence_mbar_init();
     }
     float g[CPT][8];
 #pragma unroll
@@ -422,18 +423,24 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
         if (tid == 0) {
             if (p0 > 0) fence_proxy_async_smem();  // earlier reads of the buffer come first
             const uint64_t policy = policy_evict_first();
-            mbar_arrive_expect_tx(bar_addr, n * row_bytes);
-            for (int r = 0; r < n; ++r)
+            if (!PER_ROW) mbar_arrive_expect_tx(bar_addr, n * row_bytes);
+            for (int r = 0; r < n; ++r) {
+                const uint32_t b = PER_ROW ? smem_u32(&bars[r]) : bar_addr;
+                if (PER_ROW) mbar_arrive_expect_tx(b, row_bytes);
                 bulk_copy_g2s_hint(base + r * row_bytes,
                                    a.gemm2 + static_cast<int64_t>(idx_s[order_s[p0 + r]]) * a.ld,
-                                   row_bytes, bar_addr, policy);
-        }
-        if (!mbar_wait(bar_addr, phase, a.timeout_ns)) {
-            atomicOr(a.status, kStatusWaitTimeout);
-            ok = false;
-            (void)mbar_wait(bar_addr, phase, a.timeout_ns);  // let copies in flight land
+                                   row_bytes, b, policy);
+            }
         }
         for (int r = 0; r < n; ++r) {
+            if (PER_ROW || r == 0) {
+                const uint32_t b = PER_ROW ? smem_u32(&bars[r]) : bar_addr;
+                if (!mbar_wait(b, phase, a.timeout_ns)) {
+                    atomicOr(a.status, kStatusWaitTimeout);
+                    ok = false;
+                    (void)mbar_wait(b, phase, a.timeout_ns);  // let the copies land before exit
+                }
+            }
             const float w = w_s[order_s[p0 + r]];
             const uint32_t row = base + r * row_bytes;
             uint4 q[CPT];
@@ -477,8 +484,8 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
 int generic_cpt(int hidden) { return ((hidden / 256) % 2 == 0 && hidden / 16 >= 256) ? 2 : 1; }
 
 // Shared memory for one CTA's rows, sized so that two CTAs fit an SM (1 KB
-// system reservation and the static shared memory per CTA included).
-int generic_budget(int smem_per_sm) { return smem_per_sm / 2 - 1024 - 768; }
+// system reservation and up to 1 KB of static shared memory per CTA included).
+int generic_budget(int smem_per_sm) { return smem_per_sm / 2 - 1024 - 1024; }
 
 int generic_rows(int smem_per_sm, int top_k, int hidden) {
     const int rows = generic_budget(smem_per_sm) / (hidden * 2);
@@ -499,12 +506,15 @@ cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm) {
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightBF16>, kBulkSmem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightFP32>, kBulkSmem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightPacked>, kBulkSmem);
-    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightBF16>, budget);
-    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightFP32>, budget);
-    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightPacked>, budget);
-    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightBF16>, budget);
-    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightFP32>, budget);
-    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightPacked>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightBF16, false>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightFP32, false>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightPacked, false>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightBF16, true>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightFP32, true>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightPacked, true>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightBF16, true>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightFP32, true>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightPacked, true>, budget);
     return e;
 }
 
@@ -540,22 +550,26 @@ cudaError_t launch_tp_bulk(const TpArgs &a, int wk, cudaStream_t s) {
     }
 }
 
-template <int CPT>
+template <int CPT, bool PER_ROW>
 static cudaError_t launch_generic_cpt(const TpArgs &a, int wk, int rows, cudaStream_t s) {
     const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(a.hidden / 8 / CPT);
     const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;
     const bool p = a.programmatic;
     switch (wk) {
-        case kWeightBF16: return launch_ex(tp_generic_bulk_kernel<CPT, kWeightBF16>, grid, block, bytes, s, 1, p, a, rows);
-        case kWeightPacked: return launch_ex(tp_generic_bulk_kernel<CPT, kWeightPacked>, grid, block, bytes, s, 1, p, a, rows);
-        default: return launch_ex(tp_generic_bulk_kernel<CPT, kWeightFP32>, grid, block, bytes, s, 1, p, a, rows);
+        case kWeightBF16: return launch_ex(tp_generic_bulk_kernel<CPT, kWeightBF16, PER_ROW>, grid, block, bytes, s, 1, p, a, rows);
+        case kWeightPacked: return launch_ex(tp_generic_bulk_kernel<CPT, kWeightPacked, PER_ROW>, grid, block, bytes, s, 1, p, a, rows);
+        default: return launch_ex(tp_generic_bulk_kernel<CPT, kWeightFP32, PER_ROW>, grid, block, bytes, s, 1, p, a, rows);
     }
 }
 
+// Rows of 4 KB and more (hidden >= 2048) get one mbarrier each.
+constexpr int kPerRowMinHidden = 2048;
+
 cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, cudaStream_t s) {
     const int rows = generic_rows(smem_per_sm, a.top_k, a.hidden);
-    if (generic_cpt(a.hidden) == 2) return launch_generic_cpt<2>(a, wk, rows, s);
-    return launch_generic_cpt<1>(a, wk, rows, s);
+    if (generic_cpt(a.hidden) == 2) return launch_generic_cpt<2, true>(a, wk, rows, s);  // hidden >= 4096
+    if (a.hidden >= kPerRowMinHidden) return launch_generic_cpt<1, true>(a, wk, rows, s);
+    return launch_generic_cpt<1, false>(a, wk, rows, s);
 }
 
 }  // namespace mf
