@@ -256,10 +256,10 @@ mf_status mf_selftest_wait_timeout(uint64_t timeout_ns, mf_stream_t stream);
 
 /* Programmatic dependent launch (process-wide, on by default).  When on, every
  * kernel is launched with the programmatic stream serialisation attribute: it
- * may be scheduled while the previous kernel in the stream finishes, and it
- * waits for that kernel's completion (griddepcontrol.wait) before its first
- * global-memory access, so results are the same either way; back-to-back
- * small calls lose part of their launch gap.  The setting applies to later
+ * may be scheduled before the previous kernel in the stream has fully
+ * retired, and it waits for that kernel's completion (griddepcontrol.wait)
+ * before its first global-memory access, so results are the same either way;
+ * back-to-back small calls lose part of their launch gap.  The setting applies to later
  * calls; the producer MoE op exposes the same choice as enable_pdl
  * (flashinfer.fused_moe.trtllm_fp8_per_tensor_scale_routed_moe, parameter list). */
 void mf_set_programmatic_launch(int enable);

@@ -151,7 +151,6 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
         rs = inv_rms(tot, H, a.post_eps);
     }
     beam_store<CPT>(acc, pwq, norm, rs, a.out + t * H, tid, NT);
-    pdl_trigger();
 }
 
 // Residual step of beam_moe_finalize_norm_residual_norm (residual and
@@ -327,7 +326,6 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
     } else {
         if (ok) beam_store<CPT>(acc, pwq, norm, rs, a.out + t * H, tid, NT);
     }
-    pdl_trigger();
 }
 
 // Chunks per thread of the register kernel: the largest of 4, 2, 1 that

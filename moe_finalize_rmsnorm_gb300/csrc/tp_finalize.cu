@@ -179,7 +179,6 @@ __global__ void __launch_bounds__(kChunksPerRow / CPT)
     const float r = rsqrtf(__fmaf_rn(tot, 1.0f / kTpHidden, a.eps));
 
     scale_store<CPT, NT>(acc, g, before, r, a.out + t * kTpHidden, tid);
-    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -336,7 +335,6 @@ __global__ void __launch_bounds__(kBulkThreads)
     for (int i = 0; i < NW; ++i) tot += red[i];
     const float r = rsqrtf(__fmaf_rn(tot, 1.0f / kTpHidden, a.eps));
     if (ok) scale_store<CPT, NT>(acc, g, before, r, a.out + t * kTpHidden, tid);
-    pdl_trigger();
 }
 
 // ---------------------------------------------------------------------------
@@ -477,7 +475,6 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
         }
         st_cs_16(out_row + static_cast<int64_t>(tid + c * NT) * kChunkElems, pack8_rn(y));
     }
-    pdl_trigger();
 }
 
 // 2 chunks per thread when that leaves at least 256 threads, else 1.
