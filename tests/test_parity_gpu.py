@@ -573,3 +573,36 @@ def test_residual_norm_zero_tokens(cuda_lib):
     h, n = cuda_lib.beam_moe_finalize_norm_residual_norm(
         x, torch.from_numpy(case.weights).cuda(), r, None, None, None, 1e-6, None)
     assert h.shape == (0, 256) and n.shape == (0, 256)
+
+
+# ---------------------------------------------------------------------------
+# concurrency and size
+
+def test_concurrent_calls_on_two_streams(cuda_lib):
+    # the library keeps no per-call state: two calls in flight at once on two
+    # streams (different inputs and outputs) both give the oracle's result
+    cases = [small_case(700, seed=80), si.beam_case("conc", 600, 8, 7168, 590, seed=81)]
+    tp, beam = cases
+    g, w, idx, nw = (dev_bf16(tp.gemm2), torch.from_numpy(tp.weights).cuda(),
+                     torch.from_numpy(tp.idx).cuda(), dev_bf16(tp.norm_weight))
+    x, bw, pw = (dev_bf16(beam.expert_outputs), torch.from_numpy(beam.weights).cuda(),
+                 dev_bf16(beam.post_weight))
+    out1 = torch.empty((700, 4096), dtype=torch.bfloat16, device="cuda")
+    out2 = torch.empty((590, 7168), dtype=torch.bfloat16, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(4):
+        cuda_lib.moe_finalize_rmsnorm(g, w, idx, nw, out1, eps=tp.eps, gain_center=tp.gain_center,
+                                      weight_before_norm=tp.weight_before_norm, stream=s1)
+        cuda_lib.beam_moe_finalize(x, bw, out2, beam.routed_scale, pw, beam.post_eps, stream=s2)
+    torch.cuda.synchronize()
+    compare_bf16(host_bits(out1), oracle_tp(tp))
+    compare_bf16(host_bits(out2), oracle_beam(beam))
+
+
+def test_many_tokens_small_hidden(cuda_lib):
+    # 300000 tokens (a large grid of small CTAs) on the generic path
+    T = 300_000
+    case = si.tp_case("many", T, hidden=256, top_k=8, indexed_rows=T * 8, invalid_frac=0.01,
+                      weights_dtype="bf16", seed=82)
+    compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
