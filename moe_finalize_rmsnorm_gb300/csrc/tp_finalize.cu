@@ -30,6 +30,9 @@
 //   tp_generic_bulk_kernel  any (hidden, top-k) in range: the staged design
 //                        with runtime sizes; the valid rows are copied in
 //                        pieces that fit half an SM's shared memory.
+//   tp_warp_bulk_kernel  hidden 256..1024: the staged design with one warp per
+//                        token and four tokens per CTA (small tokens would
+//                        otherwise make the grid CTA-launch bound).
 //
 // Routing weights may be BF16, FP32 or the producer's packed int32 routing
 // words (expert_id << 16) | bf16 weight bits (trtllm_fp8_per_tensor_scale_
@@ -477,6 +480,106 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
     }
 }
 
+// ---------------------------------------------------------------------------
+// small hidden (256..1024): one warp per token, four tokens per CTA
+
+// Each warp owns one token and up to 16 KB of shared memory: lane k reads slot k of
+// the route, the valid slots are compacted with a ballot, lane 0 copies up to
+// `rows_per_piece` valid rows at a time with one bulk copy per row (one
+// mbarrier per warp and piece), and the RMS is a warp reduction, so warps never
+// wait for one another.  Each lane owns CPW 16-byte chunks (hidden = 256 CPW).
+constexpr int kWarpTokensPerCta = 4;
+constexpr int kWarpSliceBytes = 16384;
+
+template <int CPW, int WK>
+__global__ void __launch_bounds__(32 * kWarpTokensPerCta)
+    tp_warp_bulk_kernel(const TpArgs a, const int rows_per_piece) {
+    // each warp's slice holds rows_per_piece rows (at most kWarpSliceBytes)
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    __shared__ uint64_t bars[kWarpTokensPerCta];
+    constexpr int H = 256 * CPW;
+    constexpr uint32_t row_bytes = H * 2;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpTokensPerCta + warp;
+    if (t >= a.num_tokens) return;
+    const int K = a.top_k;
+    const uint32_t base = smem_u32(rows_smem) + warp * rows_per_piece * row_bytes;
+    const uint32_t bar = smem_u32(&bars[warp]);
+
+    pdl_wait();
+    int my_idx = -1;
+    if (lane < K) my_idx = __ldg(a.idx + t * K + lane);
+    const bool valid = lane < K && slot_valid(my_idx, a.rows);
+    const float my_w = valid ? load_weight<WK>(a.weights, t * K + lane) : 0.f;
+    const unsigned mask = __ballot_sync(0xffffffffu, valid);
+    const int nvalid = __popc(mask);
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    float g[CPW][8];
+#pragma unroll
+    for (int c = 0; c < CPW; ++c) load_gain(a, lane + c * 32, g[c]);
+    __syncwarp();
+
+    float acc[CPW][8];
+#pragma unroll
+    for (int c = 0; c < CPW; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[c][j] = 0.f;
+    bool ok = true;
+    uint32_t phase = 0;
+    unsigned rest = mask;  // valid slots not yet consumed, ascending
+    for (int p0 = 0; p0 < nvalid; p0 += rows_per_piece, phase ^= 1u) {
+        const int n = nvalid - p0 < rows_per_piece ? nvalid - p0 : rows_per_piece;
+        if (lane == 0) {
+            if (p0 > 0) fence_proxy_async_smem();  // earlier reads of the slice come first
+            mbar_arrive_expect_tx(bar, n * row_bytes);
+        }
+        {
+            // the row indices live in lanes 0..K-1: broadcast each, lane 0 copies
+            const uint64_t policy = policy_evict_first();
+            unsigned m = rest;
+            for (int r = 0; r < n; ++r) {
+                const int k = __ffs(m) - 1;
+                m &= m - 1;
+                const int i = __shfl_sync(0xffffffffu, my_idx, k);
+                if (lane == 0)
+                    bulk_copy_g2s_hint(base + r * row_bytes, a.gemm2 + static_cast<int64_t>(i) * a.ld,
+                                       row_bytes, bar, policy);
+            }
+        }
+        if (!mbar_wait(bar, phase, a.timeout_ns)) {
+            atomicOr(a.status, kStatusWaitTimeout);
+            ok = false;
+            (void)mbar_wait(bar, phase, a.timeout_ns);  // let the copies land before exit
+        }
+        for (int r = 0; r < n; ++r) {
+            const int k = __ffs(rest) - 1;
+            rest &= rest - 1;
+            const float w = __shfl_sync(0xffffffffu, my_w, k);
+            const uint32_t row = base + r * row_bytes;
+            uint4 q[CPW];
+#pragma unroll
+            for (int c = 0; c < CPW; ++c) q[c] = lds_16(row + (lane + c * 32) * kChunkBytes);
+#pragma unroll
+            for (int c = 0; c < CPW; ++c) {
+                float x[8];
+                unpack8(q[c], x);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[c][j] = __fmaf_rn(w, x[j], acc[c][j]);
+            }
+        }
+        __syncwarp();  // the next piece reuses the slice
+    }
+
+    const bool before = a.before != 0;
+    const float tot = warp_sum(prenorm<CPW>(acc, g, before));
+    const float r = rsqrtf(__fadd_rn(__fdiv_rn(tot, static_cast<float>(H)), a.eps));
+    if (!ok) return;
+    scale_store<CPW, 32>(acc, g, before, r, a.out + t * H, lane);
+}
+
 // 2 chunks per thread when that leaves at least 256 threads, else 1.
 int generic_cpt(int hidden) { return ((hidden / 256) % 2 == 0 && hidden / 16 >= 256) ? 2 : 1; }
 
@@ -503,6 +606,19 @@ cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm) {
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightBF16>, kBulkSmem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightFP32>, kBulkSmem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightPacked>, kBulkSmem);
+    constexpr int warp_smem = kWarpSliceBytes * kWarpTokensPerCta;
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<1, kWeightBF16>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<1, kWeightFP32>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<1, kWeightPacked>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<2, kWeightBF16>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<2, kWeightFP32>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<2, kWeightPacked>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<3, kWeightBF16>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<3, kWeightFP32>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<3, kWeightPacked>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<4, kWeightBF16>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<4, kWeightFP32>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<4, kWeightPacked>, warp_smem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightBF16, false>, budget);
     if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightFP32, false>, budget);
     if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightPacked, false>, budget);
@@ -562,7 +678,30 @@ static cudaError_t launch_generic_cpt(const TpArgs &a, int wk, int rows, cudaStr
 // Rows of 4 KB and more (hidden >= 2048) get one mbarrier each.
 constexpr int kPerRowMinHidden = 2048;
 
+template <int CPW>
+static cudaError_t launch_warp_cpw(const TpArgs &a, int wk, cudaStream_t s) {
+    const int rows_fit = kWarpSliceBytes / (a.hidden * 2);
+    const int rows = rows_fit < a.top_k ? rows_fit : a.top_k;
+    const dim3 grid(static_cast<unsigned>((a.num_tokens + kWarpTokensPerCta - 1) / kWarpTokensPerCta));
+    const dim3 block(32 * kWarpTokensPerCta);
+    const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2 * kWarpTokensPerCta;
+    const bool p = a.programmatic;
+    switch (wk) {
+        case kWeightBF16: return launch_ex(tp_warp_bulk_kernel<CPW, kWeightBF16>, grid, block, bytes, s, 1, p, a, rows);
+        case kWeightPacked: return launch_ex(tp_warp_bulk_kernel<CPW, kWeightPacked>, grid, block, bytes, s, 1, p, a, rows);
+        default: return launch_ex(tp_warp_bulk_kernel<CPW, kWeightFP32>, grid, block, bytes, s, 1, p, a, rows);
+    }
+}
+
 cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, cudaStream_t s) {
+    // hidden 256..1024: one warp per token
+    switch (a.hidden) {
+        case 256: return launch_warp_cpw<1>(a, wk, s);
+        case 512: return launch_warp_cpw<2>(a, wk, s);
+        case 768: return launch_warp_cpw<3>(a, wk, s);
+        case 1024: return launch_warp_cpw<4>(a, wk, s);
+        default: break;
+    }
     const int rows = generic_rows(smem_per_sm, a.top_k, a.hidden);
     if (generic_cpt(a.hidden) == 2) return launch_generic_cpt<2, true>(a, wk, rows, s);  // hidden >= 4096
     if (a.hidden >= kPerRowMinHidden) return launch_generic_cpt<1, true>(a, wk, rows, s);

@@ -273,7 +273,8 @@ def test_non_default_stream(cuda_lib):
 # other sizes (hidden 256..8192, top_k 1..32) and packed routing words
 
 @pytest.mark.parametrize("H,K", [(256, 1), (256, 32), (7168, 8), (8192, 32), (4096, 4),
-                                 (2048, 16), (7936, 3), (1536, 5), (4096, 8)])
+                                 (2048, 16), (7936, 3), (1536, 5), (4096, 8), (512, 32),
+                                 (768, 7), (1024, 8), (1024, 32), (1280, 2)])
 @pytest.mark.parametrize("wdt", ["fp32", "bf16", "packed"])
 def test_generic_sizes(cuda_lib, H, K, wdt):
     T = 37
@@ -600,8 +601,17 @@ def test_concurrent_calls_on_two_streams(cuda_lib):
     compare_bf16(host_bits(out2), oracle_beam(beam))
 
 
+@pytest.mark.parametrize("T", [1, 3, 4, 5, 9])
+def test_warp_per_token_partial_ctas(cuda_lib, T):
+    # hidden <= 1024 runs one warp per token, four per CTA: token counts that
+    # leave the last CTA partly empty
+    case = si.tp_case("warp_partial", T, hidden=512, top_k=8, indexed_rows=T * 8 + 2,
+                      invalid_frac=0.1, weights_dtype="fp32", seed=90 + T)
+    compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
+
+
 def test_many_tokens_small_hidden(cuda_lib):
-    # 300000 tokens (a large grid of small CTAs) on the generic path
+    # 300000 tokens (a large grid) on the warp-per-token path
     T = 300_000
     case = si.tp_case("many", T, hidden=256, top_k=8, indexed_rows=T * 8, invalid_frac=0.01,
                       weights_dtype="bf16", seed=82)
