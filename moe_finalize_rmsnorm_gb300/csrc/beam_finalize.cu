@@ -17,8 +17,10 @@
 //                          with every load of a group issued before its FMAs.
 //   beam_token_bulk_kernel one CTA per live token; thread 0 copies the token's
 //                          contiguous block into shared memory with 1-D bulk
-//                          copies on one mbarrier (two CTAs per SM), then
-//                          every thread reduces its chunks from shared memory.
+//                          copies (two CTAs per SM), then every thread reduces
+//                          its chunks from shared memory.
+//   beam_warp_bulk_kernel  hidden 256..1024: the same with one warp per token,
+//                          four tokens per CTA.
 //
 // H ranges over 256..8192 in steps of 256 and K over 1..32, as the wrapper's
 // assertions allow.
@@ -161,7 +163,9 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
 // BF16(hidden * rsqrt(mean(hidden^2) + next_eps) * next_weight).  Each thread
 // reads the residual chunks it later overwrites, so hidden may be written into
 // the residual buffer itself.
-template <int CPT>
+// WARP: one warp holds the whole token (the RMS is a warp reduction, `red`
+// unused); otherwise the CTA does (a shared-memory reduction over NT/32 warps).
+template <int CPT, bool WARP = false>
 __device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const uint4 (&pwq)[CPT],
                                                   const uint4 (&resq)[CPT],
                                                   const uint4 (&nwq)[CPT], const BeamArgs &a,
@@ -188,11 +192,14 @@ __device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const uint
     }
     if (!a.has_next) return;
     ss = warp_sum(ss);
-    if ((tid & 31) == 0) red[tid >> 5] = ss;
-    __syncthreads();
-    float tot = 0.f;
-    const int nw = NT >> 5;
-    for (int i = 0; i < nw; ++i) tot += red[i];
+    float tot = ss;
+    if constexpr (!WARP) {
+        if ((tid & 31) == 0) red[tid >> 5] = ss;
+        __syncthreads();
+        tot = 0.f;
+        const int nw = NT >> 5;
+        for (int i = 0; i < nw; ++i) tot += red[i];
+    }
     const float rn = inv_rms(tot, H, a.next_eps);
     uint16_t *norm_row = a.normalized + t * H;
 #pragma unroll
@@ -328,6 +335,100 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// small hidden (256..1024): one warp per live token, four tokens per CTA
+
+// As beam_token_bulk_kernel, with one warp per token: lane 0 copies the
+// token's contiguous rows into the warp's slice of shared memory (at most
+// 16 KB, one copy and one mbarrier per piece), each lane owns CPW 16-byte
+// chunks (hidden = 256 CPW), and both RMS reductions are warp reductions.
+constexpr int kBeamWarpTokens = 4;
+constexpr int kBeamWarpSlice = 16384;
+
+template <int CPW, bool RESID>
+__global__ void __launch_bounds__(32 * kBeamWarpTokens)
+    beam_warp_bulk_kernel(const BeamArgs a, const int rows_per_piece) {
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    __shared__ uint64_t bars[kBeamWarpTokens];
+    constexpr int H = 256 * CPW;
+    constexpr uint32_t row_bytes = H * 2;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kBeamWarpTokens + warp;
+    if (t >= a.live) return;
+    const int K = a.top_k;
+    const uint32_t base = smem_u32(rows_smem) + warp * rows_per_piece * row_bytes;
+    const uint32_t bar = smem_u32(&bars[warp]);
+    const uint16_t *xt = a.x + t * K * static_cast<int64_t>(H);
+
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    pdl_wait();
+    const float wl = lane < K ? __ldg(a.weights + t * K + lane) : 0.f;
+    uint4 pwq[CPW];
+    load_post_weight<CPW>(a, lane, 32, pwq);
+    uint4 resq[CPW], nwq[CPW];
+    if constexpr (RESID) {
+#pragma unroll
+        for (int c = 0; c < CPW; ++c) {
+            const int chunk = lane + c * 32;
+            resq[c] = ld_nc_na_16(a.residual + t * H + static_cast<int64_t>(chunk) * kChunkElems);
+            nwq[c] = a.next_weight
+                         ? __ldg(reinterpret_cast<const uint4 *>(a.next_weight) + chunk)
+                         : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        }
+    }
+    __syncwarp();
+
+    float acc[CPW][8];
+#pragma unroll
+    for (int c = 0; c < CPW; ++c)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[c][j] = 0.f;
+    bool ok = true;
+    uint32_t phase = 0;
+    for (int k0 = 0; k0 < K; k0 += rows_per_piece, phase ^= 1u) {
+        const int n = K - k0 < rows_per_piece ? K - k0 : rows_per_piece;
+        if (lane == 0) {
+            if (k0 > 0) fence_proxy_async_smem();  // earlier reads of the slice come first
+            mbar_arrive_expect_tx(bar, n * row_bytes);
+            bulk_copy_g2s_hint(base, xt + static_cast<int64_t>(k0) * H, n * row_bytes, bar,
+                               policy_evict_first());
+        }
+        if (!mbar_wait(bar, phase, a.timeout_ns)) {
+            atomicOr(a.status, kStatusWaitTimeout);
+            ok = false;
+            (void)mbar_wait(bar, phase, a.timeout_ns);  // let the copy land before exit
+        }
+        for (int r = 0; r < n; ++r) {
+            const float w = __shfl_sync(0xffffffffu, wl, k0 + r);
+            const uint32_t row = base + r * row_bytes;
+            uint4 q[CPW];
+#pragma unroll
+            for (int c = 0; c < CPW; ++c) q[c] = lds_16(row + (lane + c * 32) * kChunkBytes);
+#pragma unroll
+            for (int c = 0; c < CPW; ++c) {
+                float x[8];
+                unpack8(q[c], x);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) acc[c][j] = __fmaf_rn(w, x[j], acc[c][j]);
+            }
+        }
+        __syncwarp();  // the next piece reuses the slice
+    }
+
+    round_scale_round<CPW>(acc, a.routed_scale);
+    const bool norm = a.has_norm != 0;
+    float rs = 1.f;
+    if (norm) rs = inv_rms(warp_sum(sum_squares<CPW>(acc)), H, a.post_eps);
+    if constexpr (RESID) {
+        residual_epilogue<CPW, true>(acc, pwq, resq, nwq, a, norm, rs, t, lane, 32, nullptr, ok);
+    } else {
+        if (ok) beam_store<CPW>(acc, pwq, norm, rs, a.out + t * H, lane, 32);
+    }
+}
+
 // Chunks per thread of the register kernel: the largest of 4, 2, 1 that
 // divides H/256 and leaves at least 128 threads (a multiple of 32 either way).
 int beam_cpt(int hidden) {
@@ -371,6 +472,15 @@ cudaError_t prepare_beam_kernels(int smem_per_sm) {
     const int budget = beam_bulk_budget(smem_per_sm);
     const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
     cudaError_t e = cudaSuccess;
+    const int warp_smem = kBeamWarpSlice * kBeamWarpTokens;
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_warp_bulk_kernel<1, false>, attr, warp_smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_warp_bulk_kernel<2, false>, attr, warp_smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_warp_bulk_kernel<3, false>, attr, warp_smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_warp_bulk_kernel<4, false>, attr, warp_smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_warp_bulk_kernel<1, true>, attr, warp_smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_warp_bulk_kernel<2, true>, attr, warp_smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_warp_bulk_kernel<3, true>, attr, warp_smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_warp_bulk_kernel<4, true>, attr, warp_smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, false, false>, attr, budget);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, true, false>, attr, budget);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, false, true>, attr, budget);
@@ -391,7 +501,26 @@ cudaError_t launch_beam_token_cta(const BeamArgs &a, cudaStream_t s) {
     }
 }
 
+template <int CPW>
+static cudaError_t launch_beam_warp(const BeamArgs &a, bool residual, cudaStream_t s) {
+    const int fit = kBeamWarpSlice / (a.hidden * 2);
+    const int rows = fit < a.top_k ? fit : a.top_k;
+    const dim3 grid(static_cast<unsigned>((a.live + kBeamWarpTokens - 1) / kBeamWarpTokens));
+    const dim3 block(32 * kBeamWarpTokens);
+    const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2 * kBeamWarpTokens;
+    if (residual)
+        return launch_ex(beam_warp_bulk_kernel<CPW, true>, grid, block, bytes, s, 1, a.programmatic, a, rows);
+    return launch_ex(beam_warp_bulk_kernel<CPW, false>, grid, block, bytes, s, 1, a.programmatic, a, rows);
+}
+
 cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, bool residual, cudaStream_t s) {
+    switch (a.hidden) {  // hidden 256..1024: one warp per token
+        case 256: return launch_beam_warp<1>(a, residual, s);
+        case 512: return launch_beam_warp<2>(a, residual, s);
+        case 768: return launch_beam_warp<3>(a, residual, s);
+        case 1024: return launch_beam_warp<4>(a, residual, s);
+        default: break;
+    }
     const int cpt = beam_bulk_cpt(a.hidden);
     const int rows = beam_bulk_rows(smem_per_sm, a.top_k, a.hidden);
     const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;

@@ -321,7 +321,7 @@ def test_unsupported_hidden_raises(cuda_lib):
 # edge cases: Beam
 
 @pytest.mark.parametrize("K,H", [(1, 256), (32, 256), (8, 8192), (3, 7936), (5, 1536), (32, 8192),
-                                 (2, 2560), (8, 4096)])
+                                 (2, 2560), (8, 4096), (32, 1024), (7, 768), (8, 512)])
 @pytest.mark.parametrize("variant", BEAM_VARIANTS)
 def test_beam_shapes(cuda_lib, K, H, variant):
     case = si.beam_case(f"beam_{K}_{H}", 40, K, H, 37, routed_scale=2.5, seed=K * 1000 + H,
@@ -550,7 +550,8 @@ def test_residual_norm_matches_oracle(cuda_lib, post, nxt, scales):
         assert np.array_equal(h, rh)   # no norm on the way to hidden: bit-exact
 
 
-@pytest.mark.parametrize("K,H", [(1, 256), (32, 8192), (3, 7936), (16, 2048)])
+@pytest.mark.parametrize("K,H", [(1, 256), (32, 8192), (3, 7936), (16, 2048), (32, 1024),
+                                 (5, 768)])
 def test_residual_norm_shapes_and_in_place(cuda_lib, K, H):
     cap, T = 40, 37
     case = si.beam_case("resid_shapes", cap, K, H, T, routed_scale=1.5, seed=K + H)
