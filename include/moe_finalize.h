@@ -120,8 +120,8 @@ typedef enum mf_variant {
  * sqrt(mean_h v[h]^2 + eps) over the `hidden` columns; output = BF16(y)
  * rounded to nearest even.
  *
- * Errors: MF_ERR_SHAPE (num_tokens < 0, rows < 0, row_stride < hidden or not
- * a multiple of 8), MF_ERR_UNSUPPORTED (hidden / top_k outside the sizes
+ * Errors: MF_ERR_SHAPE (num_tokens < 0 or above 2^27 - 1, rows < 0,
+ * row_stride < hidden or not a multiple of 8), MF_ERR_UNSUPPORTED (hidden / top_k outside the sizes
  * above), MF_ERR_INVALID (TOKEN_CTA or CLUSTER for sizes other than 4096 / 8),
  * MF_ERR_NULL, MF_ERR_ALIGN, MF_ERR_DTYPE, MF_ERR_CUDA.
  */
@@ -172,7 +172,7 @@ mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
  * * post_weight), else output = v.
  *
  * Errors: MF_ERR_UNSUPPORTED (top_k or hidden out of range), MF_ERR_SHAPE
- * (live_tokens < 0 or > capacity, weight_rows < live_tokens), MF_ERR_INVALID
+ * (live_tokens < 0, > capacity or above 2^31 - 1, weight_rows < live_tokens), MF_ERR_INVALID
  * (post_weight without has_post_norm), MF_ERR_NULL, MF_ERR_ALIGN, MF_ERR_CUDA.
  */
 mf_status beam_moe_finalize(const void *expert_outputs, int64_t capacity,

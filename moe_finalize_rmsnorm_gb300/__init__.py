@@ -15,7 +15,6 @@ streams.  There is no CPU fallback: without the built library the calls raise.
 """
 from __future__ import annotations
 
-import ctypes
 
 import torch
 
@@ -33,9 +32,22 @@ HIDDEN = 4096
 TOP_K = 8
 
 
-def _stream_ptr(stream, device) -> ctypes.c_void_p:
+_BF16 = torch.bfloat16
+_WEIGHT_DTYPES = {torch.bfloat16: MF_DTYPE_BF16, torch.float32: MF_DTYPE_FP32,
+                  torch.int32: MF_DTYPE_PACKED_TOPK}
+
+
+def _stream_ptr(stream, device) -> int:
     s = torch.cuda.current_stream(device) if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+    return s.cuda_stream
+
+
+def _on_device(dev: torch.device, fn, *args) -> int:
+    """Call fn with dev as the current CUDA device (switching only if needed)."""
+    if dev.index is None or dev.index == torch.cuda.current_device():
+        return fn(*args)
+    with torch.cuda.device(dev):
+        return fn(*args)
 
 
 def _req(cond: bool, msg: str) -> None:
@@ -44,8 +56,10 @@ def _req(cond: bool, msg: str) -> None:
 
 
 def _variant(name: str) -> int:
-    _req(name in VARIANTS, f"unknown variant {name!r}; one of {sorted(VARIANTS)}")
-    return VARIANTS[name]
+    v = VARIANTS.get(name)
+    if v is None:
+        raise ValueError(f"unknown variant {name!r}; one of {sorted(VARIANTS)}")
+    return v
 
 
 def moe_finalize_rmsnorm(gemm2_permuted: torch.Tensor, expert_weights: torch.Tensor,
@@ -66,31 +80,33 @@ def moe_finalize_rmsnorm(gemm2_permuted: torch.Tensor, expert_weights: torch.Ten
     """
     g, w, idx, nw, out = gemm2_permuted, expert_weights, expanded_idx_to_permuted_idx, \
         norm_weight, output
-    _req(g.dim() == 2 and g.dtype == torch.bfloat16 and (g.stride(1) == 1 or g.shape[1] <= 1),
-         "gemm2_permuted must be a 2-D BF16 tensor with unit last-dim stride")
-    _req(out.dim() == 2 and out.dtype == torch.bfloat16 and out.is_contiguous(),
-         "output must be a contiguous 2-D BF16 tensor")
-    _req(idx.dim() == 2 and idx.dtype == torch.int32 and idx.is_contiguous(),
-         "expanded_idx_to_permuted_idx must be a contiguous 2-D int32 tensor")
-    _req(w.dtype in (torch.bfloat16, torch.float32, torch.int32) and w.is_contiguous() and
-         w.shape == idx.shape,
-         "expert_weights must be contiguous BF16, FP32 or packed int32 with the index map's shape")
-    _req(nw.dim() == 1 and nw.dtype == torch.bfloat16 and nw.is_contiguous(),
-         "norm_weight must be a contiguous 1-D BF16 tensor")
-    _req(out.shape[0] == idx.shape[0], "output and the index map disagree on num_tokens")
-    _req(nw.shape[0] == out.shape[1], "norm_weight and output disagree on hidden")
+    gs, os_, ids = g.shape, out.shape, idx.shape
+    wdt = _WEIGHT_DTYPES.get(w.dtype)
+    if len(gs) != 2 or g.dtype != _BF16 or (g.stride(1) != 1 and gs[1] > 1):
+        raise ValueError("gemm2_permuted must be a 2-D BF16 tensor with unit last-dim stride")
+    if len(os_) != 2 or out.dtype != _BF16 or not out.is_contiguous():
+        raise ValueError("output must be a contiguous 2-D BF16 tensor")
+    if len(ids) != 2 or idx.dtype != torch.int32 or not idx.is_contiguous():
+        raise ValueError("expanded_idx_to_permuted_idx must be a contiguous 2-D int32 tensor")
+    if wdt is None or not w.is_contiguous() or w.shape != ids:
+        raise ValueError("expert_weights must be contiguous BF16, FP32 or packed int32 with the "
+                         "index map's shape")
+    if nw.dim() != 1 or nw.dtype != _BF16 or not nw.is_contiguous():
+        raise ValueError("norm_weight must be a contiguous 1-D BF16 tensor")
+    if os_[0] != ids[0]:
+        raise ValueError("output and the index map disagree on num_tokens")
+    if nw.shape[0] != os_[1]:
+        raise ValueError("norm_weight and output disagree on hidden")
     dev = out.device
-    _req(dev.type == "cuda" and all(t.device == dev for t in (g, w, idx, nw)),
-         "all tensors must be on the same CUDA device")
-    row_stride = g.stride(0) if g.shape[0] > 1 else max(g.shape[1], g.stride(0))
-    with torch.cuda.device(dev):
-        st = lib().moe_finalize_rmsnorm_variant(
-            g.data_ptr(), g.shape[0], row_stride, w.data_ptr(),
-            {torch.bfloat16: MF_DTYPE_BF16, torch.float32: MF_DTYPE_FP32,
-             torch.int32: MF_DTYPE_PACKED_TOPK}[w.dtype], idx.data_ptr(),
-            nw.data_ptr(), out.data_ptr(), out.shape[0], out.shape[1], idx.shape[1], float(eps),
-            float(gain_center), int(bool(weight_before_norm)), _variant(variant),
-            _stream_ptr(stream, dev))
+    if dev.type != "cuda" or g.device != dev or w.device != dev or idx.device != dev or \
+            nw.device != dev:
+        raise ValueError("all tensors must be on the same CUDA device")
+    row_stride = g.stride(0) if gs[0] > 1 else max(gs[1], g.stride(0))
+    st = _on_device(dev, lib().moe_finalize_rmsnorm_variant,
+                    g.data_ptr(), gs[0], row_stride, w.data_ptr(), wdt, idx.data_ptr(),
+                    nw.data_ptr(), out.data_ptr(), os_[0], os_[1], ids[1], float(eps),
+                    float(gain_center), 1 if weight_before_norm else 0, _variant(variant),
+                    _stream_ptr(stream, dev))
     check(st, "moe_finalize_rmsnorm")
 
 
@@ -127,11 +143,10 @@ def beam_moe_finalize(expert_outputs: torch.Tensor, expert_weights: torch.Tensor
              post_weight.dtype == torch.bfloat16 and post_weight.device == dev,
              "post_weight must be a contiguous BF16 [hidden] tensor on the output's device")
         pw_ptr = post_weight.data_ptr()
-    with torch.cuda.device(dev):
-        st = lib().beam_moe_finalize_variant(
-            x.data_ptr(), cap, w.data_ptr(), w.shape[0], out.data_ptr(), out.shape[0], top_k,
-            hidden, float(routed_scale), pw_ptr, float(post_eps or 0.0),
-            int(post_eps is not None), _variant(variant), _stream_ptr(stream, dev))
+    st = _on_device(dev, lib().beam_moe_finalize_variant,
+                    x.data_ptr(), cap, w.data_ptr(), w.shape[0], out.data_ptr(), out.shape[0],
+                    top_k, hidden, float(routed_scale), pw_ptr, float(post_eps or 0.0),
+                    int(post_eps is not None), _variant(variant), _stream_ptr(stream, dev))
     check(st, "beam_moe_finalize")
     return out
 
@@ -182,14 +197,14 @@ def beam_moe_finalize_norm_residual_norm(
             _req(o.shape == r.shape and o.dtype == torch.bfloat16 and o.is_contiguous() and
                  o.device == dev, "outputs must be contiguous BF16 like residual")
     s0, s1 = scales if scales is not None else (1.0, 1.0)
-    with torch.cuda.device(dev):
-        st = lib().beam_moe_finalize_norm_residual_norm(
-            x.data_ptr(), cap, w.data_ptr(), cap, r.data_ptr(), tokens, top_k, hid_size,
-            float(routed_scale), None if post_weight is None else post_weight.data_ptr(),
-            float(post_eps or 0.0), int(post_eps is not None),
-            None if next_weight is None else next_weight.data_ptr(), float(next_eps or 0.0),
-            int(next_eps is not None), float(s0), float(s1), hidden.data_ptr(),
-            None if normalized is None else normalized.data_ptr(), _stream_ptr(stream, dev))
+    st = _on_device(dev, lib().beam_moe_finalize_norm_residual_norm,
+                    x.data_ptr(), cap, w.data_ptr(), cap, r.data_ptr(), tokens, top_k, hid_size,
+                    float(routed_scale), None if post_weight is None else post_weight.data_ptr(),
+                    float(post_eps or 0.0), int(post_eps is not None),
+                    None if next_weight is None else next_weight.data_ptr(),
+                    float(next_eps or 0.0), int(next_eps is not None), float(s0), float(s1),
+                    hidden.data_ptr(), None if normalized is None else normalized.data_ptr(),
+                    _stream_ptr(stream, dev))
     check(st, "beam_moe_finalize_norm_residual_norm")
     return hidden, normalized
 
