@@ -86,3 +86,21 @@ def test_algorithmic_bytes_formula():
     assert si.algorithmic_bytes_tp(1) == 8 * 4096 * 2 + 4096 * 2 + 32 + 32 == 73792
     assert si.algorithmic_bytes_tp(32768) == 2418016256
     assert si.algorithmic_bytes_beam(8000, 7168, 8) == 8000 * 129056
+
+
+def test_reference_arm_prints_one_json_line():
+    # the reference arm (the oracle on the host cores) on the 16-token workload
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    p = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--workload", "small", "--steps", "3", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300, cwd=root)
+    assert p.returncode == 0, p.stderr
+    lines = [l for l in p.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["steps"] == 3 and d["warmup"] == 3
