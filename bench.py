@@ -10,7 +10,7 @@ alternates between steps so both orderings are timed.  The inputs (2.42 GB
 per call) are larger than L2, so every call reads its rows from HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload roofline|padded|beam|beam_residual|small|decode|custom]
+                    [--workload roofline|padded|beam|beam_residual|small|decode|custom|beam_custom]
                     [--tokens T]
                     [--hidden H --top-k K --weights fp32|bf16|packed]
 
@@ -225,7 +225,7 @@ def make_tp_job(torch, mf, case: si.TpCase, device, variant: str, alternate: boo
     kernel = {"bulk": "tp_token_bulk_kernel", "token_cta": "tp_token_cta_kernel",
               "cluster": "tp_cluster_kernel"}[chosen]
     if (case.hidden, case.top_k) != (4096, 8):
-        kernel = "tp_generic_bulk_kernel"
+        kernel = "tp_warp_bulk_kernel" if case.hidden <= 1024 else "tp_generic_bulk_kernel"
     job = Job(case.name, T, si.algorithmic_bytes_tp(T, case.hidden, case.top_k, wbytes), kernel,
               launch, case, {"variant": chosen})
     job.device_tensors = (g, w, idx, nw, out)
@@ -245,6 +245,8 @@ def make_beam_job(torch, mf, case: si.BeamCase, device, variant: str) -> Job:
 
     chosen = mf.select_beam_variant(case.live_tokens, K, H) if variant == "auto" else variant
     kernel = {"bulk": "beam_token_bulk_kernel", "token_cta": "beam_token_cta_kernel"}[chosen]
+    if chosen == "bulk" and H <= 1024:
+        kernel = "beam_warp_bulk_kernel"
     job = Job(case.name, case.live_tokens, si.algorithmic_bytes_beam(case.live_tokens, H, K),
               kernel, launch, case, {"variant": chosen})
     job.device_tensors = (x, w, pw, out)
@@ -302,6 +304,12 @@ def workload_case(name: str, tokens: int | None, seed_rank: int, args_hidden: in
                        gain_center=1.0, eps=1e-6, seed=seed_rank)
         return "tp", c, (f"finalize+RMSNorm num_tokens={T} hidden={H} top_k={K} "
                          f"{args_weights} weights, 1% invalid, rows={T * K} ~N(0,1)")
+    if name == "beam_custom":
+        T, H, K = tokens or 8192, args_hidden, args_top_k
+        c = si.beam_case(f"beam_T{T}_H{H}_K{K}", T, K, H, T, routed_scale=2.5, post_weight=True,
+                         post_eps=1e-6, seed=seed_rank)
+        return "beam", c, (f"Beam finalize capacity=live={T} top_k={K} hidden={H} "
+                           "routed_scale=2.5 post-RMSNorm")
     if name == "beam_residual":
         c = si.beam_8000_live(poison_dead_rows=False)
         c.meta["residual"] = si.normal_bf16((c.live_tokens, 7168), 1.0, 7, 1)
@@ -600,9 +608,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default="roofline",
                    choices=("roofline", "padded", "beam", "beam_residual", "small", "decode",
-                            "custom"))
+                            "custom", "beam_custom"))
     p.add_argument("--tokens", type=int, default=None,
-                   help="token count of --workload decode / custom")
+                   help="token count of --workload decode / custom / beam_custom")
     p.add_argument("--hidden", type=int, default=4096, help="hidden size of --workload custom")
     p.add_argument("--top-k", type=int, default=8, help="top-k of --workload custom")
     p.add_argument("--weights", default="fp32", choices=("fp32", "bf16", "packed"),
