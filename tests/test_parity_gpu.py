@@ -617,3 +617,28 @@ def test_many_tokens_small_hidden(cuda_lib):
     case = si.tp_case("many", T, hidden=256, top_k=8, indexed_rows=T * 8, invalid_frac=0.01,
                       weights_dtype="bf16", seed=82)
     compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
+
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_consumes_output_of_preceding_torch_kernels(cuda_lib, variant):
+    # PyTorch kernels (which know nothing of programmatic launch) write the rows,
+    # the index map and the weights right before the call on the same stream
+    case = small_case(256, seed=95)
+    g0 = dev_bf16(case.gemm2)
+    idx0 = torch.from_numpy(case.idx).cuda()
+    w0 = torch.from_numpy(case.weights).cuda()
+    nw = dev_bf16(case.norm_weight)
+    out = torch.empty((256, 4096), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        torch.cuda.synchronize()
+        g = g0 * 2                      # exact in BF16: an exponent step
+        idx = idx0.clone()
+        w = w0 * 1.0
+        cuda_lib.moe_finalize_rmsnorm(g, w, idx, nw, out, eps=case.eps,
+                                      gain_center=case.gain_center,
+                                      weight_before_norm=case.weight_before_norm, variant=variant)
+        torch.cuda.synchronize()
+    rows2 = f32_bits((bf16_bits_to_f64(case.gemm2) * 2).astype(np.float32))  # on the host
+    doubled = si.TpCase("doubled", rows2, case.weights, case.idx, case.norm_weight,
+                        case.hidden, case.eps, case.gain_center, case.weight_before_norm)
+    compare_bf16(host_bits(out), oracle_tp(doubled))
