@@ -367,6 +367,22 @@ def time_oracle(kind: str, case, token_lo: int, token_hi: int, threads: int,
     return time.perf_counter() - t0
 
 
+def host_cpu() -> str:
+    """CPU model and architecture of the host (for the baseline's record)."""
+    import platform
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu part", "processor name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return f"{platform.machine()} {model}".strip()
+
+
 def total_tokens(kind, case):
     return case.num_tokens if kind == "tp" else case.live_tokens
 
@@ -410,7 +426,7 @@ def run_reference(args) -> None:
         "config": {"workload": desc, "tokens_per_step": sample},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{sample} consecutive tokens of the batch per step, "
-                                   f"{threads} threads"},
+                                   f"{threads} threads", "cpu": host_cpu()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -552,10 +568,15 @@ def run_ours(args) -> None:
         T = total_tokens(kind, case)
         n = min(T, args.cpu_tokens)
         secs = time_oracle(kind, case, 0, n, threads)
+        n1 = min(n, max(1, n // 8))
+        secs1 = time_oracle(kind, case, 0, n1, 1)
         line["cpu_baseline"] = {"value": n / secs, "unit": "tokens/s", "cores": threads,
                                 "kind": "oracle",
                                 "sample": f"the first {n} tokens of the same batch, one pass, "
-                                          f"{threads} threads ({secs:.2f} s wall)"}
+                                          f"{threads} threads ({secs:.2f} s wall)",
+                                "single_thread_value": n1 / secs1,
+                                "single_thread_sample": f"the first {n1} tokens, 1 thread",
+                                "cpu": host_cpu()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
