@@ -273,6 +273,7 @@ def make_beam_residual_job(torch, mf, case: si.BeamCase, device) -> Job:
     job = Job(case.name + "_residual", T, si.algorithmic_bytes_beam_residual(T, H, K, True),
               "beam_token_bulk_kernel", launch, case, {"variant": "bulk"})
     job.device_tensors = (x, w, res, pw, nw, hid, nrm)
+    job.n_outputs = 2
     return job
 
 
@@ -585,40 +586,69 @@ def run_ours(args) -> None:
 
 def run_e2e(torch, mf, job: Job, kind: str, case, device, steps: int) -> dict:
     """Same metric through the public API with host buffers: every step copies
-    its inputs from pinned host memory and reads the result back."""
-    dev = job.device_tensors
-    host = []
-    for t in dev:
-        host.append(None if t is None else torch.empty(t.shape, dtype=t.dtype).pin_memory())
-    # host copies of the inputs (the output's host buffer receives the result)
-    for h, d in zip(host[:-1], dev[:-1]):
-        if h is not None:
-            h.copy_(d.cpu() if d.is_contiguous() else d.contiguous().cpu())
-    ins = [(h, d) for h, d in zip(host[:-1], dev[:-1]) if h is not None]
-    out_h, out_d = host[-1], dev[-1]
-    h2d = sum(h.numel() * h.element_size() for h, _ in ins)
-    d2h = out_h.numel() * out_h.element_size()
-    stream = torch.cuda.current_stream(device)
+    its inputs from pinned host memory and reads its results back.  Steps are
+    pipelined over two sets of device buffers: the upload of step i+1 runs
+    while step i computes and downloads (uploads and downloads use separate
+    streams; the host link is full duplex)."""
+    n_out = getattr(job, "n_outputs", 1)
+    dev0 = list(job.device_tensors)
+    ins_idx = [i for i, t in enumerate(dev0[:-n_out]) if t is not None]
+    outs_idx = list(range(len(dev0) - n_out, len(dev0)))
+    # pinned host buffers: inputs hold the step's data, outputs receive the results
+    host = {i: torch.empty(dev0[i].shape, dtype=dev0[i].dtype).pin_memory()
+            for i in ins_idx + outs_idx}
+    for i in ins_idx:
+        host[i].copy_(dev0[i].cpu())
+    dev1 = [None if t is None else torch.empty(t.shape, dtype=t.dtype, device=device) for t in dev0]
+    sets = [dev0, dev1]
+    h2d = sum(host[i].numel() * host[i].element_size() for i in ins_idx)
+    d2h = sum(host[i].numel() * host[i].element_size() for i in outs_idx)
+    s_in, s_cmp, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    main = torch.cuda.current_stream(device)
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    cmp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
 
     def step(i):
-        for h, d in ins:
-            d.copy_(h, non_blocking=True)
-        job.launch(i)
-        out_h.copy_(out_d, non_blocking=True)
+        b = i % 2
+        d = sets[b]
+        if i >= 2:
+            s_in.wait_event(cmp_done[b])      # step i-2 no longer reads this set
+        with torch.cuda.stream(s_in):
+            for k in ins_idx:
+                d[k].copy_(host[k], non_blocking=True)
+            in_done[b].record(s_in)
+        s_cmp.wait_event(in_done[b])
+        if i >= 2:
+            s_cmp.wait_event(out_done[b])     # step i-2's results have been read back
+        with torch.cuda.stream(s_cmp):
+            job.launch(i, tensors=tuple(d))
+            cmp_done[b].record(s_cmp)
+        s_out.wait_event(cmp_done[b])
+        with torch.cuda.stream(s_out):
+            for k in outs_idx:
+                host[k].copy_(d[k], non_blocking=True)
+            out_done[b].record(s_out)
 
-    step(0)
+    for i in range(2):  # untimed: both buffer sets touched once
+        step(i)
     torch.cuda.synchronize(device)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    start.record(stream)
+    start.record(main)
+    for st in (s_in, s_cmp, s_out):
+        st.wait_stream(main)
     for i in range(steps):
         step(i)
-    end.record(stream)
+    for st in (s_in, s_cmp, s_out):
+        main.wait_stream(st)
+    end.record(main)
     torch.cuda.synchronize(device)
     ms = reduce_max(start.elapsed_time(end))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": job.units_per_step * steps * world / (ms / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
-            "ms_per_step": ms / steps}
+            "ms_per_step": ms / steps,
+            "pipeline": "uploads, launches and downloads on three streams, two buffer sets"}
 
 
 def parse_args(argv=None):
@@ -641,7 +671,7 @@ def parse_args(argv=None):
                    help="replay the timed launches from one CUDA graph (decode sizes)")
     p.add_argument("--no-pdl", action="store_true",
                    help="launch without programmatic dependent launch")
-    p.add_argument("--e2e-steps", type=int, default=5)
+    p.add_argument("--e2e-steps", type=int, default=8)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-tokens", type=int, default=32768,

@@ -1,0 +1,104 @@
+"""Seeded random configurations of every operation and kernel against the
+oracle (GPU), and calls from several host threads at once."""
+import threading
+
+import numpy as np
+import pytest
+
+import oracle
+import synth_inputs as si
+from helpers import compare_bf16
+from test_parity_gpu import (cuda_lib, dev_bf16, host_bits, oracle_beam, oracle_tp,  # noqa: F401
+                             run_beam, run_tp)
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+def _random_tp(seed):
+    rng = np.random.default_rng(1000 + seed)
+    specialised = rng.random() < 0.5
+    H = 4096 if specialised else int(rng.integers(1, 33)) * 256
+    K = 8 if specialised else int(rng.integers(1, 33))
+    T = int(rng.choice([1, 2, 7, 33, 150, 1023, 1024, 1500]))
+    stride = H + 8 * int(rng.integers(0, 4))
+    extra_rows = int(rng.integers(0, 50))
+    case = si.tp_case(f"fuzz{seed}", T, hidden=H, top_k=K, indexed_rows=T * K + extra_rows,
+                      padding_rows=int(rng.integers(0, 5)), row_stride=stride,
+                      sigma=float(rng.choice([0.5, 1.0, 3.0])),
+                      invalid_frac=float(rng.choice([0.0, 0.05, 0.5])),
+                      weights_dtype=str(rng.choice(["fp32", "bf16", "packed"])),
+                      norm_mu=float(rng.choice([0.0, 1.0])), gain_center=float(rng.choice([0.0, 1.0, -0.5])),
+                      eps=float(rng.choice([1e-6, 1e-5, 0.1])),
+                      weight_before_norm=bool(rng.random() < 0.5), seed=seed,
+                      poison_padding=True)
+    variants = ["auto", "bulk"] + (["token_cta", "cluster"] if specialised else [])
+    return case, variants
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_fuzz_finalize(cuda_lib, seed):
+    case, variants = _random_tp(seed)
+    ref = oracle_tp(case)
+    for v in variants:
+        compare_bf16(run_tp(cuda_lib, case, v), ref)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_fuzz_beam(cuda_lib, seed):
+    rng = np.random.default_rng(2000 + seed)
+    H = int(rng.integers(1, 33)) * 256
+    K = int(rng.integers(1, 33))
+    cap = int(rng.integers(1, 200))
+    live = int(rng.integers(0, cap + 1))
+    norm = bool(rng.random() < 0.7)
+    case = si.beam_case(f"bfuzz{seed}", cap, K, H, live, routed_scale=float(rng.choice([1.0, 2.5, 0.375])),
+                        post_weight=norm and bool(rng.random() < 0.5),  # a weight needs its eps
+                        post_eps=1e-6 if norm else None,
+                        seed=seed, poison_dead_rows=True)
+    if live == 0:
+        return
+    ref = oracle_beam(case)
+    for v in ("auto", "token_cta"):
+        compare_bf16(run_beam(cuda_lib, case, v), ref)
+
+
+def test_calls_from_several_host_threads(cuda_lib):
+    # four host threads, each with its own stream and inputs, calling at once
+    cases = [small_case_for_thread(i) for i in range(4)]
+    refs = [oracle_tp(c) for c in cases]
+    results = [None] * 4
+    errors = []
+
+    def worker(i):
+        try:
+            c = cases[i]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                g, w = dev_bf16(c.gemm2), torch.from_numpy(c.weights).cuda()
+                idx, nw = torch.from_numpy(c.idx).cuda(), dev_bf16(c.norm_weight)
+                out = torch.empty((c.num_tokens, 4096), dtype=torch.bfloat16, device="cuda")
+                for _ in range(20):
+                    cuda_lib.moe_finalize_rmsnorm(g, w, idx, nw, out, eps=c.eps,
+                                                  gain_center=c.gain_center,
+                                                  weight_before_norm=c.weight_before_norm,
+                                                  stream=s)
+                s.synchronize()
+                results[i] = host_bits(out)
+        except Exception as e:  # pragma: no cover - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    for got, ref in zip(results, refs):
+        compare_bf16(got, ref)
+
+
+def small_case_for_thread(i):
+    return si.tp_case(f"thread{i}", [5, 70, 600, 1200][i], indexed_rows=[5, 70, 600, 1200][i] * 8,
+                      invalid_frac=0.05, weights_dtype="fp32", seed=300 + i,
+                      weight_before_norm=bool(i % 2))
