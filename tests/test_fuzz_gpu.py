@@ -5,14 +5,12 @@ import threading
 import numpy as np
 import pytest
 
-import oracle
 import synth_inputs as si
+from gpu_common import dev_bf16, host_bits, oracle_beam, oracle_tp, run_beam, run_tp
 from helpers import compare_bf16
-from test_parity_gpu import (cuda_lib, dev_bf16, host_bits, oracle_beam, oracle_tp,  # noqa: F401
-                             run_beam, run_tp)
 
 torch = pytest.importorskip("torch")
-pytestmark = pytest.mark.gpu
+pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
 
 
 def _random_tp(seed):
