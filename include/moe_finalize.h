@@ -2,7 +2,7 @@
  * moe_finalize.h -- C ABI of the GB300 (sm_103a) MoE finalize library
  * (libmoe_finalize.so).
  *
- * Two operations:
+ * Three operations:
  *
  *   moe_finalize_rmsnorm  -- flashinfer.comm.tp_moe_finalize_rmsnorm (API
  *     page: description and parameter list).  Per token t, gather the
@@ -15,6 +15,10 @@
  *     token-major [capacity, top_k, hidden] block in FP32, round to BF16,
  *     multiply by routed_scale and round to BF16 again, optionally apply a
  *     post-RMSNorm, write BF16.
+ *
+ *   beam_moe_finalize_norm_residual_norm -- the same page's function of that
+ *     name: the Beam finalize, then a residual add and the next RMSNorm, in one
+ *     kernel (the residual step is a reading of the pages; see its comment).
  *
  * Conventions for every entry point:
  *   - Pointers marked "device" are CUDA device (or managed) memory of the
@@ -29,7 +33,8 @@
  *     the launch error.
  *   - A token count of zero is a no-op that returns MF_OK (pointers unchecked),
  *     matching the Beam wrapper's "if output.shape[0]" guard.
- *   - The output must not alias any input.
+ *   - Outputs must not alias inputs (one exception: the residual op's hidden
+ *     output may be its residual buffer).
  *   - Kernel waits are bounded (about two seconds of wall time); a wait that
  *     gives up sets MF_ERR_DEVICE_TIMEOUT in the device status word, which
  *     mf_device_status() reads.
