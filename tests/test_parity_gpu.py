@@ -573,3 +573,32 @@ def test_consumes_output_of_preceding_torch_kernels(cuda_lib, variant):
     doubled = si.TpCase("doubled", rows2, case.weights, case.idx, case.norm_weight,
                         case.hidden, case.eps, case.gain_center, case.weight_before_norm)
     compare_bf16(host_bits(out), oracle_tp(doubled))
+
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_nan_and_inf_in_valid_rows_propagate_like_the_oracle(cuda_lib, variant):
+    # a NaN in a gathered row makes the token's mean square NaN: the whole token
+    # is NaN.  An Inf makes the mean square Inf, so 1/rms = 0: the token is 0
+    # except where its sum is Inf (Inf * 0 = NaN).  Same on both sides; tokens
+    # that do not gather those rows are unaffected.
+    case = small_case(40, seed=96)
+    g = case.gemm2.copy()
+    nan_row, inf_row = int(case.idx[3, 0]), int(case.idx[9, 2])
+    g[nan_row, 5] = 0x7FC0
+    g[inf_row, 100] = 0x7F80
+    case.gemm2 = g
+    got = run_tp(cuda_lib, case, variant)
+    ref = oracle_tp(case)
+    r9 = bf16_bits_to_f64(ref[9])
+    assert np.isnan(bf16_bits_to_f64(ref[3])).all()
+    assert np.argwhere(np.isnan(r9)).ravel().tolist() == [100] and np.all(r9[~np.isnan(r9)] == 0)
+    compare_bf16(got, ref)
+
+
+@pytest.mark.parametrize("variant", ("token_cta", "bulk", "cluster"))
+def test_subnormal_inputs(cuda_lib, variant):
+    # BF16 subnormal rows (no flush to zero on either side)
+    case = si.tp_case("subnormal", 32, indexed_rows=300, sigma=3e-39, invalid_frac=0.02,
+                      weights_dtype="fp32", seed=97, eps=1e-30)
+    assert (case.gemm2 & 0x7F80 == 0).mean() > 0.5     # mostly subnormal BF16 values
+    compare_bf16(run_tp(cuda_lib, case, variant), oracle_tp(case))
