@@ -241,13 +241,32 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
     const uint32_t base = smem_u32(rows_smem);
     const uint16_t *xt = a.x + t * K * static_cast<int64_t>(H);
 
-    // one mbarrier per buffered row: the reduction starts on a row as soon as
-    // it lands
+    // Copy k0..k0+n-1 of the token's rows into the buffer (thread 0 only).  One
+    // mbarrier per buffered row: the reduction starts on a row as soon as it
+    // lands.
+    auto issue_piece = [&](int k0, int n) {
+        const uint64_t policy = policy_evict_first();
+        if (PER_ROW) {
+            for (int r = 0; r < n; ++r) {
+                const uint32_t b = smem_u32(&bars[r]);
+                mbar_arrive_expect_tx(b, row_bytes);
+                bulk_copy_g2s_hint(base + r * row_bytes, xt + static_cast<int64_t>(k0 + r) * H,
+                                   row_bytes, b, policy);
+            }
+        } else {  // the piece's rows are contiguous: one copy
+            const uint32_t b = smem_u32(&bars[0]);
+            mbar_arrive_expect_tx(b, n * row_bytes);
+            bulk_copy_g2s_hint(base, xt + static_cast<int64_t>(k0) * H, n * row_bytes, b, policy);
+        }
+    };
+    // The rows' addresses depend on nothing the kernel reads, so thread 0 puts
+    // the first piece in flight at once.
     if (tid == 0) {
         for (int r = 0; r < (PER_ROW ? rows_per_piece : 1); ++r) mbar_init(smem_u32(&bars[r]), 1);
         fence_mbar_init();
     }
     pdl_wait();
+    if (tid == 0) issue_piece(0, K < rows_per_piece ? K : rows_per_piece);
     if (tid < K) wsm[tid] = __ldg(a.weights + t * K + tid);
     uint4 pwq[CPT];  // post_weight, fetched while the rows are in flight
     load_post_weight<CPT>(a, tid, NT, pwq);
@@ -274,22 +293,9 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
     uint32_t phase = 0;
     for (int k0 = 0; k0 < K; k0 += rows_per_piece, phase ^= 1u) {
         const int n = K - k0 < rows_per_piece ? K - k0 : rows_per_piece;
-        if (tid == 0) {
-            if (k0 > 0) fence_proxy_async_smem();  // earlier reads of the buffer come first
-            const uint64_t policy = policy_evict_first();
-            if (PER_ROW) {
-                for (int r = 0; r < n; ++r) {
-                    const uint32_t b = smem_u32(&bars[r]);
-                    mbar_arrive_expect_tx(b, row_bytes);
-                    bulk_copy_g2s_hint(base + r * row_bytes, xt + static_cast<int64_t>(k0 + r) * H,
-                                       row_bytes, b, policy);
-                }
-            } else {  // the piece's rows are contiguous: one copy
-                const uint32_t b = smem_u32(&bars[0]);
-                mbar_arrive_expect_tx(b, n * row_bytes);
-                bulk_copy_g2s_hint(base, xt + static_cast<int64_t>(k0) * H, n * row_bytes, b,
-                                   policy);
-            }
+        if (tid == 0 && k0 > 0) {
+            fence_proxy_async_smem();  // earlier reads of the buffer come first
+            issue_piece(k0, n);
         }
         for (int r = 0; r < n; ++r) {
             if (PER_ROW || r == 0) {

@@ -345,8 +345,9 @@ __global__ void __launch_bounds__(kBulkThreads)
 
 // Warp 0 reads the route (lane k holds slot k), compacts the valid slots in
 // ascending k into shared memory, and thread 0 copies up to `rows_per_piece`
-// valid rows at a time into the staging buffer with one bulk copy per row.
-// Each thread owns CPT 16-byte chunks of the H columns.  Same arithmetic as
+// valid rows at a time into the staging buffer with one bulk copy per row;
+// the first piece leaves as soon as the route is known, before the CTA's
+// barrier and the norm_weight loads.  Each thread owns CPT 16-byte chunks of the H columns.  Same arithmetic as
 // the specialised kernels: FP32 FMA over valid slots in ascending k, then the
 // RMSNorm epilogue with the mean over the H columns.
 template <int WK>
@@ -390,20 +391,41 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
     const uint32_t base = smem_u32(rows_smem);
     const uint32_t bar_addr = smem_u32(&bars[0]);
 
+    // Copy valid rows p0..p0+n-1 (in ascending slot order) into the buffer
+    // (thread 0 only).
+    auto issue_piece = [&](int p0, int n) {
+        const uint64_t policy = policy_evict_first();
+        if (!PER_ROW) mbar_arrive_expect_tx(bar_addr, n * row_bytes);
+        for (int r = 0; r < n; ++r) {
+            const uint32_t b = PER_ROW ? smem_u32(&bars[r]) : bar_addr;
+            if (PER_ROW) mbar_arrive_expect_tx(b, row_bytes);
+            bulk_copy_g2s_hint(base + r * row_bytes,
+                               a.gemm2 + static_cast<int64_t>(idx_s[order_s[p0 + r]]) * a.ld,
+                               row_bytes, b, policy);
+        }
+    };
+
     pdl_wait();
     if (tid < 32) {
         int i = -1;
-        float w = 0.f;
         if (tid < K) i = __ldg(a.idx + t * K + tid);
         const bool valid = tid < K && slot_valid(i, a.rows);
-        if (valid) w = load_weight<WK>(a.weights, t * K + tid);  // invalid slots: never read
+        // the weight (of a valid slot only) is requested before the rows, so
+        // that it does not queue behind them, and used after the copies are issued
+        const float w = valid ? load_weight<WK>(a.weights, t * K + tid) : 0.f;
         const unsigned mask = __ballot_sync(0xffffffffu, valid);
+        const int nv = __popc(mask);
         idx_s[tid] = i;
-        w_s[tid] = w;
         if (valid) order_s[__popc(mask & ((1u << tid) - 1u))] = tid;
-        if (PER_ROW ? tid < rows_per_piece : tid == 0) mbar_init(smem_u32(&bars[tid]), 1);
-        if (tid == 0) nvalid_s = __popc(mask);
-        fence_mbar_init();
+        if (tid == 0) {
+            for (int r = 0; r < (PER_ROW ? rows_per_piece : 1); ++r) mbar_init(smem_u32(&bars[r]), 1);
+            fence_mbar_init();
+            nvalid_s = nv;
+        }
+        __syncwarp();  // lane 0 reads the other lanes' idx_s / order_s
+        // the first piece goes in flight as soon as the route is known
+        if (tid == 0 && nv > 0) issue_piece(0, nv < rows_per_piece ? nv : rows_per_piece);
+        w_s[tid] = w;
     }
     float g[CPT][8];
 #pragma unroll
@@ -421,17 +443,9 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
     uint32_t phase = 0;
     for (int p0 = 0; p0 < nvalid; p0 += rows_per_piece, phase ^= 1u) {
         const int n = nvalid - p0 < rows_per_piece ? nvalid - p0 : rows_per_piece;
-        if (tid == 0) {
-            if (p0 > 0) fence_proxy_async_smem();  // earlier reads of the buffer come first
-            const uint64_t policy = policy_evict_first();
-            if (!PER_ROW) mbar_arrive_expect_tx(bar_addr, n * row_bytes);
-            for (int r = 0; r < n; ++r) {
-                const uint32_t b = PER_ROW ? smem_u32(&bars[r]) : bar_addr;
-                if (PER_ROW) mbar_arrive_expect_tx(b, row_bytes);
-                bulk_copy_g2s_hint(base + r * row_bytes,
-                                   a.gemm2 + static_cast<int64_t>(idx_s[order_s[p0 + r]]) * a.ld,
-                                   row_bytes, b, policy);
-            }
+        if (tid == 0 && p0 > 0) {
+            fence_proxy_async_smem();  // earlier reads of the buffer come first
+            issue_piece(p0, n);
         }
         for (int r = 0; r < n; ++r) {
             if (PER_ROW || r == 0) {
