@@ -437,6 +437,28 @@ def run_reference(args) -> None:
 # ---------------------------------------------------------------------------
 # the CUDA path
 
+def per_launch_pass(torch, job: Job, stream, n: int, alternating: bool) -> dict:
+    """Distribution of single-launch times, from a pass after the timed region
+    with an event pair around every launch.  The event records between
+    launches make each launch wait for the one before it to drain and expose
+    its start-up, so these read a few microseconds above the back-to-back
+    average; the headline figures do not use them."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for i in range(n):
+        ev[i][0].record(stream)
+        job.launch(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b) for a, b in ev]
+    out = {"launches": n,
+           "us_p10_p50_p90": [float(np.percentile(ms, q)) * 1e3 for q in (10, 50, 90)]}
+    if alternating and n > 1:
+        out["us_mean_by_ordering"] = {"weight_before_norm=false": statistics.fmean(ms[0::2]) * 1e3,
+                                      "weight_before_norm=true": statistics.fmean(ms[1::2]) * 1e3}
+    return out
+
+
 def run_ours(args) -> None:
     import torch
     import torch.distributed as dist
@@ -501,20 +523,16 @@ def run_ours(args) -> None:
         end.record(stream)
         torch.cuda.synchronize(device)
         t_wall1 = time.time()
-        launch_ms = [start.elapsed_time(end) / args.steps] * args.steps
     else:
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+        # the K launches back to back, as a caller issues them: nothing else on the
+        # stream between them, so the region's length / K is the average launch
         t_wall0 = time.time()
         start.record(stream)
         for i in range(args.steps):
-            ev[i][0].record(stream)
             job.launch(i)
-            ev[i][1].record(stream)
         end.record(stream)
         torch.cuda.synchronize(device)
         t_wall1 = time.time()
-        launch_ms = [a.elapsed_time(b) for a, b in ev]
     if world > 1:
         dist.barrier()
     clocks.stop()
@@ -522,7 +540,7 @@ def run_ours(args) -> None:
         raise SystemExit("device wait timeout in the timed region")
 
     elapsed_ms = reduce_max(start.elapsed_time(end))
-    avg_launch_ms = statistics.fmean(launch_ms)
+    avg_launch_ms = elapsed_ms / args.steps
     units = job.units_per_step * args.steps * world
     value = units / (elapsed_ms / 1e3)
     hbm_gbs = job.bytes_per_launch * args.steps / (elapsed_ms / 1e3) / 1e9
@@ -530,12 +548,11 @@ def run_ours(args) -> None:
     achieved = job.bytes_per_launch / (avg_launch_ms / 1e3) / 1e9
     traffic = recorded_traffic(job.kernel, job.name)
     extra = {}
-    if args.workload == "roofline":
-        extra["launch_us_by_ordering"] = {
-            "weight_before_norm=false": statistics.fmean(launch_ms[0::2]) * 1e3,
-            "weight_before_norm=true": statistics.fmean(launch_ms[1::2]) * 1e3
-            if len(launch_ms) > 1 else None}
-    extra["launch_us_p10_p50_p90"] = [float(np.percentile(launch_ms, q)) * 1e3 for q in (10, 50, 90)]
+    if not args.graph:
+        extra["per_launch_events"] = per_launch_pass(torch, job, stream, min(args.steps, 400),
+                                                     args.workload == "roofline")
+        if mf.device_status(clear=True) != 0:
+            raise SystemExit("device wait timeout in the per-launch pass")
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -548,7 +565,7 @@ def run_ours(args) -> None:
                    if job.bytes_per_launch > 256e6 else "inputs smaller than L2 (warm)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "timing": "one CUDA graph of all timed launches" if args.graph
-                   else "CUDA events around every launch",
+                   else "one CUDA event pair around the K back-to-back launches",
                    "programmatic_dependent_launch": not args.no_pdl,
                    **job.describe},
         "hbm_gbs": hbm_gbs,
