@@ -347,7 +347,8 @@ __global__ void __launch_bounds__(kBulkThreads)
 // ascending k into shared memory, and thread 0 copies up to `rows_per_piece`
 // valid rows at a time into the staging buffer with one bulk copy per row;
 // the first piece leaves as soon as the route is known, before the CTA's
-// barrier and the norm_weight loads.  Each thread owns CPT 16-byte chunks of the H columns.  Same arithmetic as
+// barrier and the norm_weight loads, each of its rows (of 4 KB and more)
+// issued by the lane of its slot.  Each thread owns CPT 16-byte chunks of the H columns.  Same arithmetic as
 // the specialised kernels: FP32 FMA over valid slots in ascending k, then the
 // RMSNorm epilogue with the mean over the H columns.
 template <int WK>
@@ -392,7 +393,7 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
     const uint32_t bar_addr = smem_u32(&bars[0]);
 
     // Copy valid rows p0..p0+n-1 (in ascending slot order) into the buffer
-    // (thread 0 only).
+    // (thread 0: the pieces after the first, and the first one for small rows).
     auto issue_piece = [&](int p0, int n) {
         const uint64_t policy = policy_evict_first();
         if (!PER_ROW) mbar_arrive_expect_tx(bar_addr, n * row_bytes);
@@ -415,16 +416,31 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
         const float w = valid ? load_weight<WK>(a.weights, t * K + tid) : 0.f;
         const unsigned mask = __ballot_sync(0xffffffffu, valid);
         const int nv = __popc(mask);
+        const int rank = __popc(mask & ((1u << tid) - 1u));
         idx_s[tid] = i;
-        if (valid) order_s[__popc(mask & ((1u << tid) - 1u))] = tid;
-        if (tid == 0) {
-            for (int r = 0; r < (PER_ROW ? rows_per_piece : 1); ++r) mbar_init(smem_u32(&bars[r]), 1);
-            fence_mbar_init();
-            nvalid_s = nv;
+        if (valid) order_s[rank] = tid;
+        if (PER_ROW) {
+            // the lane of the rank-th valid slot owns row `rank` of the first
+            // piece: it initialises and arms that row's mbarrier and copies its
+            // own row, so the first piece's copies leave together
+            if (valid && rank < rows_per_piece) {
+                const uint32_t b = smem_u32(&bars[rank]);
+                mbar_init(b, 1);
+                fence_mbar_init();
+                mbar_arrive_expect_tx(b, row_bytes);
+                bulk_copy_g2s_hint(base + rank * row_bytes, a.gemm2 + static_cast<int64_t>(i) * a.ld,
+                                   row_bytes, b, policy_evict_first());
+            }
+            if (tid == 0) nvalid_s = nv;
+        } else {  // small rows: one mbarrier for the piece, thread 0 copies
+            if (tid == 0) {
+                mbar_init(bar_addr, 1);
+                fence_mbar_init();
+                nvalid_s = nv;
+            }
+            __syncwarp();
+            if (tid == 0 && nv > 0) issue_piece(0, nv < rows_per_piece ? nv : rows_per_piece);
         }
-        __syncwarp();  // lane 0 reads the other lanes' idx_s / order_s
-        // the first piece goes in flight as soon as the route is known
-        if (tid == 0 && nv > 0) issue_piece(0, nv < rows_per_piece ? nv : rows_per_piece);
         w_s[tid] = w;
     }
     float g[CPT][8];
