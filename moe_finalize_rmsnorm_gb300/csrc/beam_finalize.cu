@@ -241,9 +241,9 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
     const uint32_t base = smem_u32(rows_smem);
     const uint16_t *xt = a.x + t * K * static_cast<int64_t>(H);
 
-    // Copy k0..k0+n-1 of the token's rows into the buffer (thread 0 only).  One
-    // mbarrier per buffered row: the reduction starts on a row as soon as it
-    // lands.
+    // Copy k0..k0+n-1 of the token's rows into the buffer (thread 0: the pieces
+    // after the first, and the first one for small rows).  One mbarrier per
+    // buffered row: the reduction starts on a row as soon as it lands.
     auto issue_piece = [&](int k0, int n) {
         const uint64_t policy = policy_evict_first();
         if (PER_ROW) {
@@ -259,14 +259,31 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
             bulk_copy_g2s_hint(base, xt + static_cast<int64_t>(k0) * H, n * row_bytes, b, policy);
         }
     };
-    // The rows' addresses depend on nothing the kernel reads, so thread 0 puts
-    // the first piece in flight at once.
-    if (tid == 0) {
-        for (int r = 0; r < (PER_ROW ? rows_per_piece : 1); ++r) mbar_init(smem_u32(&bars[r]), 1);
-        fence_mbar_init();
+    // The rows' addresses depend on nothing the kernel reads, so the first
+    // piece goes in flight at once: with per-row barriers lane r of warp 0
+    // initialises and arms row r's mbarrier and copies row r (all in parallel),
+    // otherwise thread 0 copies the piece.
+    const int n0 = K < rows_per_piece ? K : rows_per_piece;
+    if (PER_ROW) {
+        if (tid < rows_per_piece) {
+            mbar_init(smem_u32(&bars[tid]), 1);
+            fence_mbar_init();
+        }
+        pdl_wait();
+        if (tid < n0) {
+            const uint32_t b = smem_u32(&bars[tid]);
+            mbar_arrive_expect_tx(b, row_bytes);
+            bulk_copy_g2s_hint(base + tid * row_bytes, xt + static_cast<int64_t>(tid) * H, row_bytes, b,
+                               policy_evict_first());
+        }
+    } else {
+        if (tid == 0) {
+            mbar_init(smem_u32(&bars[0]), 1);
+            fence_mbar_init();
+        }
+        pdl_wait();
+        if (tid == 0) issue_piece(0, n0);
     }
-    pdl_wait();
-    if (tid == 0) issue_piece(0, K < rows_per_piece ? K : rows_per_piece);
     if (tid < K) wsm[tid] = __ldg(a.weights + t * K + tid);
     uint4 pwq[CPT];  // post_weight, fetched while the rows are in flight
     load_post_weight<CPT>(a, tid, NT, pwq);
