@@ -48,6 +48,10 @@ PROFILES = os.path.join(ROOT, "profiles")
 # ---------------------------------------------------------------------------
 # host-side helpers (also exercised by the CPU tests)
 
+# Twice the GB300's 129 MB L2 (rounded up): the scratch write of --cold.
+L2_FLUSH_BYTES = 288 * 1024 * 1024
+
+
 def rank_seed(base_seed: int, rank: int) -> int:
     """Each rank finalizes its own independent batch (weak scaling)."""
     return base_seed + 1000003 * rank
@@ -505,7 +509,26 @@ def run_ours(args) -> None:
         dist.barrier()
     torch.cuda.synchronize(device)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if args.graph:
+    cold_ms = None
+    if args.cold:
+        # a write of twice the L2 size before every launch evicts the inputs and
+        # the previous output; each launch is timed between its own event pair
+        scratch = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        t_wall0 = time.time()
+        start.record(stream)
+        for i in range(args.steps):
+            scratch.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            job.launch(i)
+            ev[i][1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(device)
+        t_wall1 = time.time()
+        cold_ms = [a.elapsed_time(b) for a, b in ev]
+        del scratch
+    elif args.graph:
         # decode sizes: the K launches replay from one CUDA graph, so the timed
         # region holds no host launch gaps (the per-launch figure is the mean)
         graph = torch.cuda.CUDAGraph()
@@ -539,7 +562,8 @@ def run_ours(args) -> None:
     if mf.device_status(clear=True) != 0:
         raise SystemExit("device wait timeout in the timed region")
 
-    elapsed_ms = reduce_max(start.elapsed_time(end))
+    # the timed work: the K launches (with --cold, the launches alone, not the flushes)
+    elapsed_ms = reduce_max(sum(cold_ms) if cold_ms is not None else start.elapsed_time(end))
     avg_launch_ms = elapsed_ms / args.steps
     units = job.units_per_step * args.steps * world
     value = units / (elapsed_ms / 1e3)
@@ -548,7 +572,10 @@ def run_ours(args) -> None:
     achieved = job.bytes_per_launch / (avg_launch_ms / 1e3) / 1e9
     traffic = recorded_traffic(job.kernel, job.name)
     extra = {}
-    if not args.graph:
+    if cold_ms is not None:
+        extra["cold_launch_us_p10_p50_p90"] = [float(np.percentile(cold_ms, q)) * 1e3
+                                               for q in (10, 50, 90)]
+    elif not args.graph:
         extra["per_launch_events"] = per_launch_pass(torch, job, stream, min(args.steps, 400),
                                                      args.workload == "roofline")
         if mf.device_status(clear=True) != 0:
@@ -560,12 +587,15 @@ def run_ours(args) -> None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": desc, "global_batch": job.units_per_step * world,
-                   "l2": "no flush: every step reads its inputs from HBM "
-                         f"({job.bytes_per_launch / 1e9:.3f} GB per launch, L2 is 0.13 GB)"
-                   if job.bytes_per_launch > 256e6 else "inputs smaller than L2 (warm)",
+                   "l2": (f"flushed before every launch ({L2_FLUSH_BYTES / 1e6:.0f} MB scratch "
+                          "write, not timed)") if args.cold else
+                         ("no flush: every step reads its inputs from HBM "
+                          f"({job.bytes_per_launch / 1e9:.3f} GB per launch, L2 is 0.13 GB)"
+                          if job.bytes_per_launch > 256e6 else "inputs smaller than L2 (warm)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "timing": "one CUDA graph of all timed launches" if args.graph
-                   else "one CUDA event pair around the K back-to-back launches",
+                   else ("an event pair around each launch, summed" if args.cold
+                         else "one CUDA event pair around the K back-to-back launches"),
                    "programmatic_dependent_launch": not args.no_pdl,
                    **job.describe},
         "hbm_gbs": hbm_gbs,
@@ -688,6 +718,9 @@ def parse_args(argv=None):
                    help="replay the timed launches from one CUDA graph (decode sizes)")
     p.add_argument("--no-pdl", action="store_true",
                    help="launch without programmatic dependent launch")
+    p.add_argument("--cold", action="store_true",
+                   help="before every timed launch write a scratch buffer of twice the L2 "
+                        "size, and time each launch alone (cold-cache latency at small sizes)")
     p.add_argument("--e2e-steps", type=int, default=8)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -695,6 +728,8 @@ def parse_args(argv=None):
                    help="tokens of the batch the CPU oracle baseline processes")
     a = p.parse_args(argv)
     a.warmup = max(3, a.warmup)  # at least three untimed warm-up steps
+    if a.cold and a.graph:
+        p.error("--cold times every launch alone; it cannot be combined with --graph")
     return a
 
 
