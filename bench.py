@@ -48,7 +48,7 @@ PROFILES = os.path.join(ROOT, "profiles")
 # ---------------------------------------------------------------------------
 # host-side helpers (also exercised by the CPU tests)
 
-# Twice the GB300's 129 MB L2 (rounded up): the scratch write of --cold.
+# More than twice the GB300's 129 MB L2: the scratch write of --cold.
 L2_FLUSH_BYTES = 288 * 1024 * 1024
 
 
