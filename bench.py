@@ -392,6 +392,16 @@ def total_tokens(kind, case):
     return case.num_tokens if kind == "tp" else case.live_tokens
 
 
+def bytes_per_token(kind, case) -> float:
+    """Algorithmic bytes per token of the workload (the roofline's count)."""
+    if kind == "tp":
+        return si.algorithmic_bytes_tp(1, case.hidden, case.top_k, case.weights.dtype.itemsize)
+    _, K, H = case.expert_outputs.shape
+    if kind == "beam_residual":
+        return si.algorithmic_bytes_beam_residual(1, H, K, True)
+    return si.algorithmic_bytes_beam(1, H, K)
+
+
 def run_reference(args) -> None:
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -431,7 +441,8 @@ def run_reference(args) -> None:
         "config": {"workload": desc, "tokens_per_step": sample},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{sample} consecutive tokens of the batch per step, "
-                                   f"{threads} threads", "cpu": host_cpu()},
+                                   f"{threads} threads",
+                         "host_gbs": value * bytes_per_token(kind, case) / 1e9, "cpu": host_cpu()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -624,6 +635,7 @@ def run_ours(args) -> None:
                                           f"{threads} threads ({secs:.2f} s wall)",
                                 "single_thread_value": n1 / secs1,
                                 "single_thread_sample": f"the first {n1} tokens, 1 thread",
+                                "host_gbs": n / secs * bytes_per_token(kind, case) / 1e9,
                                 "cpu": host_cpu()}
     if rank == 0:
         print(json.dumps(line), flush=True)
