@@ -235,9 +235,14 @@ mf_status beam_moe_finalize_norm_residual_norm(
     float next_eps, int has_next_norm, float scale_x, float scale_residual, void *hidden_out,
     void *normalized_out, mf_stream_t stream);
 
-/* The kernel AUTO would run for moe_finalize_rmsnorm with these sizes
- * (MF_VARIANT_AUTO if none would run: no tokens or unsupported sizes).  Sizes
- * other than 4096 / 8 always run the generic bulk-staged kernel (MF_VARIANT_BULK). */
+/* The kernel AUTO would run for moe_finalize_rmsnorm with these sizes on the
+ * calling thread's current device (MF_VARIANT_AUTO if none would run: no
+ * tokens or unsupported sizes).  At 4096 / 8: the cluster kernel up to 8
+ * tokens, the bulk-staged kernel from 1024; in between the register kernel
+ * (MF_VARIANT_TOKEN_CTA) unless the bulk-staged kernel covers the tokens in
+ * fewer waves of resident CTAs (the device's SM count times each kernel's CTAs
+ * per SM).  Without a usable device the wave test is skipped.  Sizes other than
+ * 4096 / 8 always run the generic bulk-staged kernel (MF_VARIANT_BULK). */
 mf_variant mf_select_finalize_variant(int64_t num_tokens, int32_t hidden, int32_t top_k);
 
 /* The kernel AUTO would run for beam_moe_finalize. */

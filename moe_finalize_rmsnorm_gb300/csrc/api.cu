@@ -23,6 +23,8 @@ struct DeviceInfo {
     int num_sms = 0;
     int smem_optin = 0;
     int smem_per_sm = 0;
+    int bulk_per_sm = 0;       // resident CTAs per SM of the staged hidden-4096 kernel
+    int token_cta_per_sm = 0;  // and of the register kernel
     unsigned *status = nullptr;  // device address of g_status_word
 };
 
@@ -46,7 +48,8 @@ mf_status device_info(const DeviceInfo **out) {
             cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_status_word) !=
                 cudaSuccess ||
             mf::prepare_tp_kernels(d.smem_optin, d.smem_per_sm) != cudaSuccess ||
-            mf::prepare_beam_kernels(d.smem_per_sm) != cudaSuccess) {
+            mf::prepare_beam_kernels(d.smem_per_sm) != cudaSuccess ||
+            mf::tp_blocks_per_sm(&d.bulk_per_sm, &d.token_cta_per_sm) != cudaSuccess) {
             (void)cudaGetLastError();
             return MF_ERR_CUDA;
         }
@@ -64,15 +67,29 @@ bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 //                         L2, as right after the producing GEMM, against
 //                         2.61 us for one CTA per token);
 //   <  kBulkMinTokens     register kernel (one dependent index load, then all
-//                         row loads at once);
+//                         row loads at once), unless the bulk-staged kernel,
+//                         with more CTAs per SM (3 against 2 on GB300), covers
+//                         the tokens in fewer waves (384 tokens: 4.15 against
+//                         4.72 us; 768: 7.05 against 7.70 us; at 512, two
+//                         waves each, 6.32 against 5.75 us);
 //   otherwise             bulk-staged kernel (more bytes in flight per SM).
 constexpr int64_t kClusterMaxTokens = 8;
 constexpr int64_t kBulkMinTokens = 1024;
 
-mf_variant pick_tp(int64_t num_tokens) {
+int64_t waves(int64_t tokens, int64_t ctas_per_wave) {
+    return ctas_per_wave > 0 ? (tokens + ctas_per_wave - 1) / ctas_per_wave : 0;
+}
+
+// `d` may be null (no device information): the token-count rule alone.
+mf_variant pick_tp(int64_t num_tokens, const DeviceInfo *d) {
     if (num_tokens <= 0) return MF_VARIANT_AUTO;
     if (num_tokens <= kClusterMaxTokens) return MF_VARIANT_CLUSTER;
-    return num_tokens < kBulkMinTokens ? MF_VARIANT_TOKEN_CTA : MF_VARIANT_BULK;
+    if (num_tokens >= kBulkMinTokens) return MF_VARIANT_BULK;
+    if (d != nullptr && d->bulk_per_sm > 0 && d->token_cta_per_sm > 0 &&
+        waves(num_tokens, int64_t{d->bulk_per_sm} * d->num_sms) <
+            waves(num_tokens, int64_t{d->token_cta_per_sm} * d->num_sms))
+        return MF_VARIANT_BULK;
+    return MF_VARIANT_TOKEN_CTA;
 }
 
 // Beam: one CTA per live token with the token's block staged in shared memory.
@@ -162,7 +179,7 @@ mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     if (!specialised) return from_launch(mf::launch_tp_generic(a, wk, d->smem_per_sm, s));
-    if (variant == MF_VARIANT_AUTO) variant = pick_tp(num_tokens);
+    if (variant == MF_VARIANT_AUTO) variant = pick_tp(num_tokens, d);
     switch (variant) {
         case MF_VARIANT_CLUSTER: return from_launch(mf::launch_tp_cluster(a, wk, s));
         case MF_VARIANT_TOKEN_CTA: return from_launch(mf::launch_tp_token_cta(a, wk, s));
@@ -294,7 +311,11 @@ mf_status beam_moe_finalize_norm_residual_norm(
 
 mf_variant mf_select_finalize_variant(int64_t num_tokens, int32_t hidden, int32_t top_k) {
     if (num_tokens <= 0) return MF_VARIANT_AUTO;
-    if (hidden == mf::kTpHidden && top_k == mf::kTpTopK) return pick_tp(num_tokens);
+    if (hidden == mf::kTpHidden && top_k == mf::kTpTopK) {
+        const DeviceInfo *d = nullptr;
+        if (device_info(&d) != MF_OK) d = nullptr;
+        return pick_tp(num_tokens, d);
+    }
     if (hidden < 256 || hidden > 8192 || hidden % 256 != 0 || top_k < 1 || top_k > 32)
         return MF_VARIANT_AUTO;
     return MF_VARIANT_BULK;

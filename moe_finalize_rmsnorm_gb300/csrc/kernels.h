@@ -64,6 +64,9 @@ struct BeamArgs {
 // device's opt-in shared memory per block, `smem_per_sm` its shared memory
 // per multiprocessor.
 cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm);
+// CTAs per SM of the staged (bulk) and register (token_cta) hidden-4096 kernels,
+// from the occupancy calculator (after prepare_tp_kernels).
+cudaError_t tp_blocks_per_sm(int *bulk, int *token_cta);
 cudaError_t prepare_beam_kernels(int smem_per_sm);
 
 // Hidden 4096, top-k 8.

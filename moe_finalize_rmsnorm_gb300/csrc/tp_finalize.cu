@@ -669,6 +669,15 @@ cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm) {
     return e;
 }
 
+cudaError_t tp_blocks_per_sm(int *bulk, int *token_cta) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        bulk, tp_token_bulk_kernel<kWeightFP32>, kBulkThreads, kBulkSmem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(token_cta, tp_token_cta_kernel<1, kWeightFP32>,
+                                                          kChunksPerRow, 0);
+    return e;
+}
+
 cudaError_t launch_tp_token_cta(const TpArgs &a, int wk, cudaStream_t s) {
     constexpr int CPT = 1;
     const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(kChunksPerRow / CPT);

@@ -61,6 +61,27 @@ def test_finalize_decode_sizes(cuda_lib, T, variant):
     compare_bf16(run_tp(cuda_lib, case, variant), oracle_tp(case))
 
 
+def test_automatic_choice_by_waves(cuda_lib):
+    # between 9 and 1023 tokens the register kernel (2 CTAs per SM) runs unless
+    # the bulk-staged kernel (3 CTAs per SM) needs fewer waves of the device's SMs
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    def waves(t, per_sm):
+        return -(-t // (per_sm * sms))
+    for T in (1, 8, 9, 100, 2 * sms, 2 * sms + 1, 3 * sms, 3 * sms + 1, 4 * sms, 5 * sms,
+              1023, 1024, 5000):
+        if T <= 8:
+            want = "cluster"
+        elif T >= 1024:
+            want = "bulk"
+        else:
+            want = "bulk" if waves(T, 3) < waves(T, 2) else "token_cta"
+        assert cuda_lib.select_finalize_variant(T) == want, T
+    for T in (2 * sms + 1, 5 * sms):   # one token count of each choice, against the oracle
+        case = si.tp_case(f"waves_{T}", T, indexed_rows=T * 8 + 9, invalid_frac=0.02,
+                          weights_dtype="fp32", seed=T)
+        compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
+
+
 @functools.lru_cache(maxsize=1)
 def c_roofline():
     return si.finalize_32768_tokens(weight_before_norm=False)
