@@ -514,14 +514,14 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
 // small hidden (256..1024): one warp per token, four tokens per CTA
 
 // Each warp owns one token and up to 16 KB of shared memory: lane k reads slot k of
-// the route, the valid slots are compacted with a ballot, lane 0 copies up to
-// `rows_per_piece` valid rows at a time with one bulk copy per row (one
-// mbarrier per warp and piece), and the RMS is a warp reduction, so warps never
+// the route, the valid slots are compacted with a ballot, and up to
+// `rows_per_piece` valid rows at a time are copied with one bulk copy per row,
+// each issued by the lane of its slot (one mbarrier per warp and piece), and the RMS is a warp reduction, so warps never
 // wait for one another.  Each lane owns CPW 16-byte chunks (hidden = 256 CPW).
-// Tokens per CTA: four at hidden 256, two from 512 up (measured: at 512 and 768
-// two per CTA are about 4 % faster than four, at 256 about 3 % slower).
+// Two tokens per CTA (measured against four and eight: the same or faster at
+// every hidden size, 5 % at 256 x 32 and 4 % at 768; eight up to 25 % slower).
 template <int CPW>
-constexpr int warp_tokens_per_cta() { return CPW == 1 ? 4 : 2; }
+constexpr int warp_tokens_per_cta() { return 2; }
 constexpr int kWarpSliceBytes = 16384;
 
 template <int CPW, int WK>
@@ -547,6 +547,7 @@ __global__ void __launch_bounds__(32 * warp_tokens_per_cta<CPW>())
     const float my_w = valid ? load_weight<WK>(a.weights, t * K + lane) : 0.f;
     const unsigned mask = __ballot_sync(0xffffffffu, valid);
     const int nvalid = __popc(mask);
+    const int my_rank = __popc(mask & ((1u << lane) - 1u));
     if (lane == 0) {
         mbar_init(bar, 1);
         fence_mbar_init();
@@ -566,23 +567,14 @@ __global__ void __launch_bounds__(32 * warp_tokens_per_cta<CPW>())
     unsigned rest = mask;  // valid slots not yet consumed, ascending
     for (int p0 = 0; p0 < nvalid; p0 += rows_per_piece, phase ^= 1u) {
         const int n = nvalid - p0 < rows_per_piece ? nvalid - p0 : rows_per_piece;
-        if (lane == 0) {
-            if (p0 > 0) fence_proxy_async_smem();  // earlier reads of the slice come first
-            mbar_arrive_expect_tx(bar, n * row_bytes);
-        }
-        {
-            // the row indices live in lanes 0..K-1: broadcast each, lane 0 copies
-            const uint64_t policy = policy_evict_first();
-            unsigned m = rest;
-            for (int r = 0; r < n; ++r) {
-                const int k = __ffs(m) - 1;
-                m &= m - 1;
-                const int i = __shfl_sync(0xffffffffu, my_idx, k);
-                if (lane == 0)
-                    bulk_copy_g2s_hint(base + r * row_bytes, a.gemm2 + static_cast<int64_t>(i) * a.ld,
-                                       row_bytes, bar, policy);
-            }
-        }
+        if (p0 > 0) fence_proxy_async_smem();  // earlier reads of the slice come first
+        if (lane == 0) mbar_arrive_expect_tx(bar, n * row_bytes);
+        __syncwarp();
+        // the lane of each valid slot in the piece copies its own row (all at once)
+        if (valid && my_rank >= p0 && my_rank < p0 + n)
+            bulk_copy_g2s_hint(base + (my_rank - p0) * row_bytes,
+                               a.gemm2 + static_cast<int64_t>(my_idx) * a.ld, row_bytes, bar,
+                               policy_evict_first());
         if (!mbar_wait(bar, phase, a.timeout_ns)) {
             atomicOr(a.status, kStatusWaitTimeout);
             ok = false;

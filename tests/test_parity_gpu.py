@@ -557,8 +557,8 @@ def test_concurrent_calls_on_two_streams(cuda_lib):
 @pytest.mark.parametrize("hidden", [256, 512])
 @pytest.mark.parametrize("T", [1, 3, 4, 5, 9])
 def test_warp_per_token_partial_ctas(cuda_lib, T, hidden):
-    # hidden <= 1024 runs one warp per token, four per CTA at hidden 256 and two
-    # from 512 up: token counts that leave the last CTA partly empty
+    # hidden <= 1024 runs one warp per token, two per CTA: token counts that leave
+    # the last CTA partly empty
     case = si.tp_case("warp_partial", T, hidden=hidden, top_k=8, indexed_rows=T * 8 + 2,
                       invalid_frac=0.1, weights_dtype="fp32", seed=90 + T)
     compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
