@@ -15,12 +15,13 @@
 //   beam_token_cta_kernel  one CTA per live token, H/8/CPT threads, each owning
 //                          CPT 16-byte chunks; slots are loaded in groups of 8
 //                          with every load of a group issued before its FMAs.
-//   beam_token_bulk_kernel one CTA per live token; thread 0 copies the token's
-//                          contiguous block into shared memory with 1-D bulk
-//                          copies (two CTAs per SM), then every thread reduces
-//                          its chunks from shared memory.
-//   beam_warp_bulk_kernel  hidden 256..1024: the same with one warp per token,
-//                          four tokens per CTA.
+//   beam_token_bulk_kernel one CTA per live token; the token's contiguous block
+//                          goes into shared memory by 1-D bulk copies, one per
+//                          row, issued by lanes of warp 0 right after the
+//                          dependency wait (two CTAs per SM), then every thread
+//                          reduces its chunks from shared memory.
+//   beam_warp_bulk_kernel  hidden 256..1024: the same with one warp per token
+//                          (one copy per piece of rows), four tokens per CTA.
 //
 // H ranges over 256..8192 in steps of 256 and K over 1..32, as the wrapper's
 // assertions allow.
@@ -217,12 +218,12 @@ __device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const uint
 // ---------------------------------------------------------------------------
 // one CTA per live token, the token's rows staged in shared memory
 
-// Thread 0 moves the token's rows with one bulk copy per row into a buffer of
-// as many whole rows as fit half an SM's shared memory (all 8 rows, 114,688 B,
-// at H = 7168), each row completing on its own mbarrier.  Data in flight holds
-// no registers, and two CTAs per SM keep two tokens' blocks in flight while
-// one of them reduces.  Rows beyond one piece are copied piece by piece into
-// the same buffer.
+// The token's rows move with one bulk copy per row into a buffer of as many
+// whole rows as fit half an SM's shared memory (all 8 rows, 114,688 B, at
+// H = 7168), each row completing on its own mbarrier; lane r of warp 0 issues
+// row r of the first piece.  Data in flight holds no registers, and two CTAs
+// per SM keep two tokens' blocks in flight while one of them reduces.  Rows
+// beyond one piece are copied piece by piece into the same buffer by thread 0.
 // PER_ROW: one mbarrier per buffered row (rows of 4 KB and more); otherwise
 // one copy and one mbarrier per piece (small rows).
 template <int CPT, bool RESID, bool PER_ROW>

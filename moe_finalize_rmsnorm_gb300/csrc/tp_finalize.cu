@@ -29,10 +29,12 @@
 //                        CTAs (192 KB of rows) fit per SM.
 //   tp_generic_bulk_kernel  any (hidden, top-k) in range: the staged design
 //                        with runtime sizes; the valid rows are copied in
-//                        pieces that fit half an SM's shared memory.
+//                        pieces that fit half an SM's shared memory, the first
+//                        piece's rows each by the lane of its slot.
 //   tp_warp_bulk_kernel  hidden 256..1024: the staged design with one warp per
-//                        token and four tokens per CTA (small tokens would
-//                        otherwise make the grid CTA-launch bound).
+//                        token and two tokens per CTA (small tokens would
+//                        otherwise make the grid CTA-launch bound); each
+//                        valid slot's lane copies its own row.
 //
 // Routing weights may be BF16, FP32 or the producer's packed int32 routing
 // words (expert_id << 16) | bf16 weight bits (trtllm_fp8_per_tensor_scale_
@@ -252,8 +254,8 @@ __global__ void __launch_bounds__(kChunksPerRow / C) tp_cluster_kernel(const TpA
 // one CTA per token, rows staged in shared memory by bulk copies
 
 // Thread 0 copies every valid row of the token (8 KB each) into its slot of a
-// 64 KB shared-memory buffer with one-dimensional bulk copies that complete on
-// a single mbarrier; the data in flight holds no registers, so three CTAs
+// 64 KB shared-memory buffer with one-dimensional bulk copies, each completing
+// on the row's own mbarrier; the data in flight holds no registers, so three CTAs
 // (192 KB of rows) can be in flight per SM.  Every thread then waits on the
 // barrier, reads its CPT chunks of each valid row from shared memory and runs
 // the same FMA chain and epilogue as the register kernel.
@@ -343,13 +345,14 @@ __global__ void __launch_bounds__(kBulkThreads)
 // ---------------------------------------------------------------------------
 // any hidden / top-k: one CTA per token, valid rows staged in pieces
 
-// Warp 0 reads the route (lane k holds slot k), compacts the valid slots in
-// ascending k into shared memory, and thread 0 copies up to `rows_per_piece`
-// valid rows at a time into the staging buffer with one bulk copy per row;
-// the first piece leaves as soon as the route is known, before the CTA's
-// barrier and the norm_weight loads, each of its rows (of 4 KB and more)
-// issued by the lane of its slot.  Each thread owns CPT 16-byte chunks of the H columns.  Same arithmetic as
-// the specialised kernels: FP32 FMA over valid slots in ascending k, then the
+// Warp 0 reads the route (lane k holds slot k) and compacts the valid slots in
+// ascending k into shared memory; up to `rows_per_piece` valid rows at a time
+// go into the staging buffer with one bulk copy per row.  The first piece
+// leaves as soon as the route is known, before the CTA's barrier and the
+// norm_weight loads, each of its rows (of 4 KB and more) issued by the lane of
+// its slot; thread 0 issues the later pieces (and small rows).  Each thread
+// owns CPT 16-byte chunks of the H columns.  Same arithmetic as the
+// specialised kernels: FP32 FMA over valid slots in ascending k, then the
 // RMSNorm epilogue with the mean over the H columns.
 template <int WK>
 __device__ __forceinline__ float load_weight(const void *weights, int64_t i) {
@@ -513,11 +516,12 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
 // ---------------------------------------------------------------------------
 // small hidden (256..1024): one warp per token, four tokens per CTA
 
-// Each warp owns one token and up to 16 KB of shared memory: lane k reads slot k of
-// the route, the valid slots are compacted with a ballot, and up to
+// Each warp owns one token and up to 16 KB of shared memory: lane k reads slot
+// k of the route, the valid slots are compacted with a ballot, and up to
 // `rows_per_piece` valid rows at a time are copied with one bulk copy per row,
-// each issued by the lane of its slot (one mbarrier per warp and piece), and the RMS is a warp reduction, so warps never
-// wait for one another.  Each lane owns CPW 16-byte chunks (hidden = 256 CPW).
+// each issued by the lane of its slot (one mbarrier per warp and piece).  The
+// RMS is a warp reduction, so warps never wait for one another.  Each lane
+// owns CPW 16-byte chunks (hidden = 256 CPW).
 // Two tokens per CTA (measured against four and eight: the same or faster at
 // every hidden size, 5 % at 256 x 32 and 4 % at 768; eight up to 25 % slower).
 template <int CPW>
