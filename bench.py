@@ -692,6 +692,16 @@ def run_e2e(torch, mf, job: Job, kind: str, case, device, steps: int) -> dict:
     for i in range(2):  # untimed: both buffer sets touched once
         step(i)
     torch.cuda.synchronize(device)
+    # the host link on its own: one plain upload of the largest input (context
+    # for the e2e figure, which the uploads bound)
+    big = max(ins_idx, key=lambda k: host[k].numel() * host[k].element_size())
+    nbytes = host[big].numel() * host[big].element_size()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    dev1[big].copy_(host[big], non_blocking=True)
+    e1.record(main)
+    torch.cuda.synchronize(device)
+    link_gbs = nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(main)
     for st in (s_in, s_cmp, s_out):
@@ -707,6 +717,7 @@ def run_e2e(torch, mf, job: Job, kind: str, case, device, steps: int) -> dict:
     return {"value": job.units_per_step * steps * world / (ms / 1e3), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": ms / steps,
+            "h2d_link_gbs": link_gbs,
             "pipeline": "uploads, launches and downloads on three streams, two buffer sets"}
 
 
