@@ -32,7 +32,7 @@
  *     non-MF_OK return nothing was launched, except MF_ERR_CUDA, which reports
  *     the launch error.
  *   - A token count of zero is a no-op that returns MF_OK (pointers unchecked),
- *     matching the Beam wrapper's "if output.shape[0]" guard.
+ *     as the Beam wrapper skips the native call when the output has no rows.
  *   - Outputs must not alias inputs (one exception: the residual op's hidden
  *     output may be its residual buffer).
  *   - Kernel waits are bounded (about two seconds of wall time); a wait that
@@ -150,8 +150,9 @@ mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
 
 /*
  * beam_moe_finalize -- vllm.models.beam.nvidia.moe_finalize, beam_moe_finalize
- * (docstring: "reduce only output rows, preserving BF16 casts before scale
- * and RMSNorm"; source: the argument assertions and the native call).
+ * (docstring: only the output rows are reduced, with BF16 rounds kept before
+ * the scale and before the norm; source: the argument assertions and the
+ * native call).
  *
  *   expert_outputs   device, BF16 [capacity, top_k, hidden] contiguous,
  *                    token-major, 16-byte aligned.  Rows t >= live_tokens are
@@ -207,9 +208,9 @@ mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity
  *   normalized = BF16(hidden / sqrt(mean(hidden^2) + next_eps) * next_weight)
  *                when has_next_norm (unweighted if next_weight is NULL)
  *
- * The residual step stands for the unfused reference's call
- * beam_norm_residual_norm(finalized, residual, None, None, next_weight,
- * next_eps, scales), whose body the pages do not show: this reading of it
+ * The residual step stands for the unfused reference's beam_norm_residual_norm,
+ * given the finalized rows, the residual, next_weight, next_eps and scales,
+ * whose body the pages do not show: this reading of it
  * (scales = (scale_x, scale_residual), (1, 1) when the caller has none) is
  * partly unpinned.
  *

@@ -1,7 +1,8 @@
 // Beam finalize kernels (sm_103a).
 //
-// Operation (vllm.models.beam.nvidia.moe_finalize, beam_moe_finalize:
-// "reduce only output rows, preserving BF16 casts before scale and RMSNorm"):
+// Operation (vllm.models.beam.nvidia.moe_finalize, beam_moe_finalize: only the
+// output rows are reduced, and the BF16 rounds before the scale and before the
+// norm are kept):
 //   s[h] = sum_k w[t,k] * x[t,k,h]         FP32 FMA chain, ascending k
 //   r    = BF16(s)                          first round
 //   v    = BF16(float(r) * routed_scale)    FP32 product, second round

@@ -26,21 +26,22 @@
  *               output = bf16(y);  otherwise output = v
  *     only rows t < live_tokens are produced.
  *
- * Precision.  The API page fixes FP32 for the routing reduction ("converted to
- * FP32 registers and remains FP32 through the routing reduction"), so the
+ * Precision.  The API page fixes FP32 for the routing reduction (the rows are
+ * widened to FP32 and the weighted sum stays in FP32), so the
  * reduction runs in float with slots in ascending order, one fused
  * multiply-add (C99 fmaf, single rounding) per slot.  The pages fix no
  * precision for the normalisation, so it runs in double (float64), and the
  * result is rounded once from double to BF16, round-to-nearest-even.  For the
- * Beam scale, the docstring's "multiplier applied after rounding the expert
- * reduction" on a BF16 tensor is read as PyTorch's BF16-tensor-times-scalar:
- * an FP32 product rounded to BF16.
+ * Beam scale, which the docstring applies to the expert reduction once it has
+ * been rounded to BF16, the product is read as PyTorch's BF16 tensor times a
+ * scalar: an FP32 product rounded to BF16.
  *
  *   vllm.models.beam.nvidia.moe_finalize, beam_moe_finalize_norm_residual_norm
  *   (docstring and source): the Beam finalize above (with its optional post
  *   norm) followed, for the same live rows, by the residual step of the unfused
- *   reference, beam_norm_residual_norm(finalized, residual, None, None,
- *   next_weight, next_eps, scales).  That function is not shown on the pages,
+ *   reference, which hands the finalized rows, the residual, next_weight,
+ *   next_eps and scales to beam_norm_residual_norm.  That function is not shown
+ *   on the pages,
  *   so this step is PARTLY UNPINNED; it is read as
  *     hidden     = BF16(s0 * finalized + s1 * residual)   FP32: one product,
  *                  then one fused multiply-add, scales (s0, s1) = (1, 1) when

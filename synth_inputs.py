@@ -10,7 +10,7 @@ shape only, not on how many threads draw them.
 The workloads mirror the shapes and distributions of the pages' operation:
 
 * flashinfer.comm.tp_moe_finalize_rmsnorm: hidden 4096, top-k 8, BF16 GEMM2
-  rows in "physical expert order" with optional padding rows and a padded row
+  rows grouped by expert (the permuted layout) with optional padding rows and a padded row
   stride (a multiple of 8 elements), an int32 index map with negative or
   out-of-range entries, BF16 or FP32 routing weights, a BF16 norm weight.
 * beam_moe_finalize: token-major BF16 [capacity, top_k, hidden], FP32
