@@ -190,3 +190,23 @@ def test_residual_norm_validation(lib):
     assert resid(lib, nrm=MIS) == ALIGN
     assert resid(lib, nw=MIS) == ALIGN
     assert resid(lib, x=None, w=None, r=None, hid=None, nrm=None, T=0) == OK
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # the product path has no CPU fallback: without the built library every
+    # entry point raises instead of computing anything
+    import torch
+    import moe_finalize_rmsnorm_gb300 as mf
+    from moe_finalize_rmsnorm_gb300 import _abi
+    monkeypatch.setattr(_abi, "_lib", None)
+    monkeypatch.setattr(_abi, "LIB", str(tmp_path / "libmoe_finalize.so"))
+    with pytest.raises(ImportError, match="no CPU fallback"):
+        _abi.lib()
+    with pytest.raises(ImportError):
+        mf.select_finalize_variant(32768)
+    g = torch.zeros((16, 4096), dtype=torch.bfloat16)
+    with pytest.raises((ImportError, ValueError, RuntimeError)):
+        mf.moe_finalize_rmsnorm(g, torch.ones((2, 8)), torch.zeros((2, 8), dtype=torch.int32),
+                                torch.ones(4096, dtype=torch.bfloat16),
+                                torch.empty((2, 4096), dtype=torch.bfloat16),
+                                eps=1e-6, gain_center=0.0, weight_before_norm=False)
