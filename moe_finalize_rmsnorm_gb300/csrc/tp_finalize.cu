@@ -349,8 +349,8 @@ __global__ void __launch_bounds__(kBulkThreads)
 // ascending k into shared memory; up to `rows_per_piece` valid rows at a time
 // go into the staging buffer with one bulk copy per row.  The first piece
 // leaves as soon as the route is known, before the CTA's barrier and the
-// norm_weight loads, each of its rows (of 4 KB and more) issued by the lane of
-// its slot; thread 0 issues the later pieces (and small rows).  Each thread
+// norm_weight loads, each of its rows issued by the lane of
+// its slot; thread 0 issues the later pieces.  Each thread
 // owns CPT 16-byte chunks of the H columns.  Same arithmetic as the
 // specialised kernels: FP32 FMA over valid slots in ascending k, then the
 // RMSNorm epilogue with the mean over the H columns.
@@ -374,8 +374,8 @@ template <int CPT>
 constexpr int generic_min_blocks() { return CPT == 2 ? 2 : 1; }
 
 // PER_ROW: one mbarrier per buffered row, so the reduction starts on a row as
-// soon as it lands (rows of 4 KB and more); otherwise one per piece (small
-// rows, where a wait per row costs more than it overlaps).
+// soon as it lands; otherwise one per piece (small rows with many slots, where
+// a wait per row costs more than it overlaps).
 template <int CPT, int WK, bool PER_ROW>
 __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks<CPT>())
     tp_generic_bulk_kernel(const TpArgs a, const int rows_per_piece) {
@@ -396,7 +396,7 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
     const uint32_t bar_addr = smem_u32(&bars[0]);
 
     // Copy valid rows p0..p0+n-1 (in ascending slot order) into the buffer
-    // (thread 0: the pieces after the first, and the first one for small rows).
+    // (thread 0, for the pieces after the first).
     auto issue_piece = [&](int p0, int n) {
         const uint64_t policy = policy_evict_first();
         if (!PER_ROW) mbar_arrive_expect_tx(bar_addr, n * row_bytes);
@@ -435,14 +435,18 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
                                    row_bytes, b, policy_evict_first());
             }
             if (tid == 0) nvalid_s = nv;
-        } else {  // small rows: one mbarrier for the piece, thread 0 copies
+        } else {  // small rows, many slots: one mbarrier for the piece, each
+                  // row still issued by the lane of its slot
             if (tid == 0) {
                 mbar_init(bar_addr, 1);
                 fence_mbar_init();
                 nvalid_s = nv;
+                if (nv > 0) mbar_arrive_expect_tx(bar_addr, (nv < rows_per_piece ? nv : rows_per_piece) * row_bytes);
             }
             __syncwarp();
-            if (tid == 0 && nv > 0) issue_piece(0, nv < rows_per_piece ? nv : rows_per_piece);
+            if (valid && rank < rows_per_piece)
+                bulk_copy_g2s_hint(base + rank * row_bytes, a.gemm2 + static_cast<int64_t>(i) * a.ld,
+                                   row_bytes, bar_addr, policy_evict_first());
         }
         w_s[tid] = w;
     }
@@ -718,8 +722,12 @@ static cudaError_t launch_generic_cpt(const TpArgs &a, int wk, int rows, cudaStr
     }
 }
 
-// Rows of 4 KB and more (hidden >= 2048) get one mbarrier each.
+// One mbarrier per row for rows of 4 KB and more (hidden >= 2048), and for
+// smaller rows when top_k <= 16 (hidden 1280-1792 x 8: 0.99 of the copy peak
+// against 0.94-0.96 with one barrier per piece); with more slots of small rows
+// one barrier per piece measured faster (1536 x 32: 167.6 against 173.3 us).
 constexpr int kPerRowMinHidden = 2048;
+constexpr int kPerRowMaxTopK = 16;
 
 template <int CPW>
 static cudaError_t launch_warp_cpw(const TpArgs &a, int wk, cudaStream_t s) {
@@ -748,7 +756,8 @@ cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, cudaStre
     }
     const int rows = generic_rows(smem_per_sm, a.top_k, a.hidden);
     if (generic_cpt(a.hidden) == 2) return launch_generic_cpt<2, true>(a, wk, rows, s);  // hidden >= 2048
-    if (a.hidden >= kPerRowMinHidden) return launch_generic_cpt<1, true>(a, wk, rows, s);
+    if (a.hidden >= kPerRowMinHidden || a.top_k <= kPerRowMaxTopK)
+        return launch_generic_cpt<1, true>(a, wk, rows, s);
     return launch_generic_cpt<1, false>(a, wk, rows, s);
 }
 

@@ -226,7 +226,8 @@ def test_non_default_stream(cuda_lib):
 
 @pytest.mark.parametrize("H,K", [(256, 1), (256, 32), (7168, 8), (8192, 32), (4096, 4),
                                  (2048, 16), (7936, 3), (1536, 5), (4096, 8), (512, 32),
-                                 (768, 7), (1024, 8), (1024, 32), (1280, 2)])
+                                 (768, 7), (1024, 8), (1024, 32), (1280, 2), (1536, 32),
+                                 (1792, 20)])
 @pytest.mark.parametrize("wdt", ["fp32", "bf16", "packed"])
 def test_generic_sizes(cuda_lib, H, K, wdt):
     T = 37
