@@ -219,12 +219,12 @@ __device__ __forceinline__ void residual_epilogue(float (&v)[CPT][8], const uint
 // ---------------------------------------------------------------------------
 // one CTA per live token, the token's rows staged in shared memory
 
-// The token's rows move with one bulk copy per row into a buffer of as many
-// whole rows as fit half an SM's shared memory (all 8 rows, 114,688 B, at
-// H = 7168), each row completing on its own mbarrier; lane r of warp 0 issues
-// row r of the first piece.  Data in flight holds no registers, and two CTAs
-// per SM keep two tokens' blocks in flight while one of them reduces.  Rows
-// beyond one piece are copied piece by piece into the same buffer by thread 0.
+// The token's rows move with one bulk copy per row into a buffer of one piece
+// of rows (beam_bulk_rows: all 8 rows, 114,688 B, at H = 7168 and top_k 8),
+// each row completing on its own mbarrier; lane r of warp 0 issues row r of the
+// first piece.  Data in flight holds no registers, and two CTAs per SM keep two
+// tokens' blocks in flight while one of them reduces.  Rows beyond one piece
+// are copied piece by piece into the same buffer by thread 0.
 // PER_ROW: one mbarrier per buffered row (rows of 4 KB and more); otherwise
 // one copy and one mbarrier per piece (small rows).
 template <int CPT, bool RESID, bool PER_ROW>
@@ -475,8 +475,15 @@ int beam_bulk_cpt(int hidden) {
 // memory: barriers, reduction and weight arrays).
 int beam_bulk_budget(int smem_per_sm) { return smem_per_sm / 2 - 1024 - 1024; }
 
+// Rows per piece: at least 8 (a whole token at top_k <= 8), otherwise pieces
+// sized so that eight CTAs fit an SM, never more than half an SM's shared
+// memory (2048 x 32: 1.05 of the copy peak against 0.80 with pieces of half an
+// SM; 1280 x 32 1.03 against 0.84; the 8-slot sizes do not change).
 int beam_bulk_rows(int smem_per_sm, int top_k, int hidden) {
-    const int rows = beam_bulk_budget(smem_per_sm) / (hidden * 2);
+    int rows = (smem_per_sm / 8 - 2048) / (hidden * 2);
+    if (rows < 8) rows = 8;
+    const int half = beam_bulk_budget(smem_per_sm) / (hidden * 2);
+    if (rows > half) rows = half;
     return rows < 1 ? 1 : (rows > top_k ? top_k : rows);
 }
 

@@ -29,8 +29,9 @@
 //                        CTAs (192 KB of rows) fit per SM.
 //   tp_generic_bulk_kernel  any (hidden, top-k) in range: the staged design
 //                        with runtime sizes; the valid rows are copied in
-//                        pieces that fit half an SM's shared memory, the first
-//                        piece's rows each by the lane of its slot.
+//                        pieces of at least 8 rows (at most half an SM's
+//                        shared memory), the first piece's rows each by the
+//                        lane of its slot.
 //   tp_warp_bulk_kernel  hidden 256..1024: the staged design with one warp per
 //                        token and two tokens per CTA (small tokens would
 //                        otherwise make the grid CTA-launch bound); each
@@ -624,8 +625,17 @@ int generic_cpt(int hidden) { return ((hidden / 256) % 2 == 0 && hidden / 16 >= 
 // system reservation and up to 1 KB of static shared memory per CTA included).
 int generic_budget(int smem_per_sm) { return smem_per_sm / 2 - 1024 - 1024; }
 
+// Rows per piece: at least 8 (a whole token at top_k <= 8), otherwise pieces
+// sized so that eight CTAs fit an SM, and never more than half an SM's shared
+// memory.  With many slots, small pieces keep more tokens in flight per SM and
+// let one piece's reduction overlap other CTAs' copies: 2048 x 32 1.04 of the
+// copy peak against 0.80 with pieces of half an SM, 1536 x 32 1.00 against
+// 0.73, 2560 x 24 1.03 against 0.85; the 8-slot sizes do not change.
 int generic_rows(int smem_per_sm, int top_k, int hidden) {
-    const int rows = generic_budget(smem_per_sm) / (hidden * 2);
+    int rows = (smem_per_sm / 8 - 2048) / (hidden * 2);
+    if (rows < 8) rows = 8;
+    const int half = generic_budget(smem_per_sm) / (hidden * 2);
+    if (rows > half) rows = half;
     return rows < 1 ? 1 : (rows > top_k ? top_k : rows);
 }
 
@@ -748,17 +758,6 @@ static cudaError_t launch_warp_cpw(const TpArgs &a, int wk, cudaStream_t s) {
     }
 }
 
-// Rows per piece for rows under 4 KB (hidden 1280..1792): pieces sized so that
-// eight CTAs fit an SM, and at least 8 rows, so that more tokens are in flight
-// per SM and each piece's reduction overlaps other CTAs' copies.  Measured
-// against pieces of half an SM: 1536 x 32 1.01 of the copy peak against 0.73,
-// 1280 x 32 0.96 against 0.62, 1536 x 16 0.98 against 0.91.
-static int small_rows(int smem_per_sm, int top_k, int hidden) {
-    int r = (smem_per_sm / 8 - 2048) / (hidden * 2);
-    if (r < 8) r = 8;
-    return r > top_k ? top_k : r;
-}
-
 cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, cudaStream_t s) {
     // hidden 256..1024: one warp per token
     switch (a.hidden) {
@@ -770,10 +769,9 @@ cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, cudaStre
     }
     const int rows = generic_rows(smem_per_sm, a.top_k, a.hidden);
     if (generic_cpt(a.hidden) == 2) return launch_generic_cpt<2, true>(a, wk, rows, s);  // hidden >= 2048
-    if (a.hidden >= kPerRowMinHidden) return launch_generic_cpt<1, true>(a, wk, rows, s);
-    if (a.top_k <= kPerRowMaxTopK)
-        return launch_generic_cpt<1, true>(a, wk, small_rows(smem_per_sm, a.top_k, a.hidden), s);
-    return launch_generic_cpt<1, false>(a, wk, small_rows(smem_per_sm, a.top_k, a.hidden), s);
+    if (a.hidden >= kPerRowMinHidden || a.top_k <= kPerRowMaxTopK)
+        return launch_generic_cpt<1, true>(a, wk, rows, s);
+    return launch_generic_cpt<1, false>(a, wk, rows, s);
 }
 
 }  // namespace mf
