@@ -274,7 +274,9 @@ def test_unsupported_hidden_raises(cuda_lib):
 # edge cases: Beam
 
 @pytest.mark.parametrize("K,H", [(1, 256), (32, 256), (8, 8192), (3, 7936), (5, 1536), (32, 8192),
-                                 (2, 2560), (8, 4096), (32, 1024), (7, 768), (8, 512)])
+                                 (2, 2560), (8, 4096), (32, 1024), (7, 768), (8, 512),
+                                 # several pieces per token: per-row barriers, then small rows
+                                 (16, 2048), (24, 3072), (32, 1536)])
 @pytest.mark.parametrize("variant", BEAM_VARIANTS)
 def test_beam_shapes(cuda_lib, K, H, variant):
     case = si.beam_case(f"beam_{K}_{H}", 40, K, H, 37, routed_scale=2.5, seed=K * 1000 + H,
