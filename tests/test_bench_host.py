@@ -80,6 +80,25 @@ def test_parse_args_defaults_and_warmup_floor():
     assert bench.parse_args(["--warmup", "1"]).warmup == 3
 
 
+def test_cold_mode_arguments():
+    a = bench.parse_args(["--workload", "decode", "--tokens", "8", "--cold"])
+    assert a.cold and not a.graph
+    # twice the 129 MB L2 at least, so one write evicts every input
+    assert bench.L2_FLUSH_BYTES >= 2 * 129 * 10 ** 6
+    with pytest.raises(SystemExit):
+        bench.parse_args(["--cold", "--graph"])
+
+
+def test_bytes_per_token_matches_the_workload_formulas():
+    import synth_inputs as si
+    kind, case, _ = bench.workload_case("small", None, 0)
+    assert bench.bytes_per_token(kind, case) == si.algorithmic_bytes_tp(1) == 73792
+    beam = si.beam_case("b", 4, 8, 7168, 3, seed=1)
+    assert bench.bytes_per_token("beam", beam) == 129056
+    assert bench.bytes_per_token("beam_residual", beam) == si.algorithmic_bytes_beam_residual(
+        1, 7168, 8, True)
+
+
 def test_algorithmic_bytes_formula():
     import synth_inputs as si
     # K*H*2 + H*2 + K*4 + K*4 per token with FP32 weights
