@@ -1,5 +1,9 @@
 """Seeded random configurations of every operation and kernel against the
-oracle (GPU), and calls from several host threads at once."""
+oracle (GPU), and calls from several host threads at once.
+
+MF_FUZZ_SEEDS=N runs N seeds of each random test instead of the default
+counts (a wide sweep: MF_FUZZ_SEEDS=300 python -m pytest tests/test_fuzz_gpu.py)."""
+import os
 import threading
 
 import numpy as np
@@ -11,6 +15,10 @@ from helpers import compare_bf16
 
 torch = pytest.importorskip("torch")
 pytestmark = [pytest.mark.gpu, pytest.mark.usefixtures("cuda_lib")]
+
+
+def _seeds(default):
+    return range(int(os.environ.get("MF_FUZZ_SEEDS", default)))
 
 
 def _random_tp(seed):
@@ -34,7 +42,7 @@ def _random_tp(seed):
     return case, variants
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", _seeds(32))
 def test_fuzz_finalize(cuda_lib, seed):
     case, variants = _random_tp(seed)
     ref = oracle_tp(case)
@@ -42,7 +50,7 @@ def test_fuzz_finalize(cuda_lib, seed):
         compare_bf16(run_tp(cuda_lib, case, v), ref)
 
 
-@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("seed", _seeds(24))
 def test_fuzz_beam(cuda_lib, seed):
     rng = np.random.default_rng(2000 + seed)
     H = int(rng.integers(1, 33)) * 256
@@ -59,6 +67,37 @@ def test_fuzz_beam(cuda_lib, seed):
     ref = oracle_beam(case)
     for v in ("auto", "token_cta"):
         compare_bf16(run_beam(cuda_lib, case, v), ref)
+
+
+@pytest.mark.parametrize("seed", _seeds(16))
+def test_fuzz_residual_norm(cuda_lib, seed):
+    import oracle
+    import test_parity_gpu as tpg
+    rng = np.random.default_rng(3000 + seed)
+    H = int(rng.integers(1, 33)) * 256
+    K = int(rng.integers(1, 33))
+    T = int(rng.integers(1, 160))
+    post = bool(rng.random() < 0.7)
+    nxt = [None, "weighted", "plain"][int(rng.integers(0, 3))]
+    scales = None if rng.random() < 0.5 else (float(rng.choice([0.5, 1.25, -0.75])),
+                                               float(rng.choice([2.0, 1.0, -0.5])))
+    case = si.beam_case(f"rfuzz{seed}", T + int(rng.integers(0, 5)), K, H, T,
+                        routed_scale=float(rng.choice([1.0, 2.5])), seed=seed)
+    res = si.normal_bf16((T, H), float(rng.choice([0.5, 2.0])), seed, 9)
+    h, n, _ = tpg.run_residual(cuda_lib, case, res, post=post, nxt=nxt, scales=scales,
+                               inplace=bool(rng.random() < 0.3))
+    nw = case.post_weight[::-1].copy() if nxt == "weighted" else None
+    rh, rn = oracle.beam_moe_finalize_norm_residual_norm(
+        case.expert_outputs, case.weights, res, routed_scale=case.routed_scale,
+        post_weight=case.post_weight if post else None, post_eps=1e-6 if post else None,
+        next_weight=nw, next_eps=1e-5 if nxt else None, scales=scales)
+    eh, en = tpg.residual_bounds(case, rh, rn, post=post, scales=scales, next_eps=1e-5,
+                                 next_weight=nw)
+    compare_bf16(h, rh, extra=eh)
+    if nxt:
+        compare_bf16(n, rn, extra=en)
+    if not post:
+        assert np.array_equal(h, rh)   # no norm on the way to hidden: bit-exact
 
 
 def test_calls_from_several_host_threads(cuda_lib):
