@@ -184,6 +184,18 @@ __device__ __forceinline__ void cluster_barrier() {
             : "memory");
 }
 
+// The same barrier with a relaxed arrive: it orders none of this thread's
+// earlier memory operations for the other CTAs, so it does not wait for
+// outstanding global stores to drain.  For the end of a cluster kernel, where
+// the barrier only keeps a CTA's shared memory alive until every peer has
+// consumed what it read from it (the values read must already be in use).
+__device__ __forceinline__ void cluster_barrier_exit() {
+    asm volatile(
+        "barrier.cluster.arrive.relaxed.aligned;\n\t"
+        "barrier.cluster.wait.aligned;" ::
+            : "memory");
+}
+
 // Load a float from the same shared-memory offset in CTA `rank` of the cluster.
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
     uint32_t remote;

@@ -248,7 +248,10 @@ __global__ void __launch_bounds__(kChunksPerRow / C) tp_cluster_kernel(const TpA
 
     scale_store<1, 1>(acc, g, before, r, a.out + t * kTpHidden, chunk);
     pdl_trigger();
-    cluster_barrier();  // no CTA leaves while another may still read its `part`
+    // no CTA leaves while another may still read its `part`; every value read
+    // from a peer has been used above, and no peer reads the stores, so the
+    // arrive is relaxed (4-6 % less per decode call than release / acquire)
+    cluster_barrier_exit();
 }
 
 // ---------------------------------------------------------------------------
