@@ -92,10 +92,6 @@ __device__ __forceinline__ void fence_mbar_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                  "r"(bytes)
@@ -132,18 +128,9 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // One-dimensional bulk copy global -> this CTA's shared memory, completing
-// `bytes` of transaction count on mbarrier `bar`.  Both addresses 16-byte
-// aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                              uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-// Same, with an L2 eviction-priority policy (evict-first for rows read once).
+// `bytes` of transaction count on mbarrier `bar`, with an L2 eviction-priority
+// policy (evict-first for rows read once).  Both addresses 16-byte aligned,
+// bytes a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s_hint(uint32_t dst, const void *src, uint32_t bytes,
                                                    uint32_t bar, uint64_t policy) {
     asm volatile(
