@@ -197,9 +197,10 @@ mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity
 
 /*
  * beam_moe_finalize_norm_residual_norm -- vllm.models.beam.nvidia.moe_finalize,
- * beam_moe_finalize_norm_residual_norm (docstring: "finalize local MegaMoE
- * tokens through the next normalization boundary"; source: the assertions and
- * the unfused reference), on one GPU.  For each of the first `tokens` rows:
+ * beam_moe_finalize_norm_residual_norm (docstring: the local tokens are
+ * carried from the finalize up to the following normalisation; source: the
+ * assertions and the unfused reference), on one GPU.  For each of the first
+ * `tokens` rows:
  *
  *   f          = the beam_moe_finalize result for the row (above), including
  *                its optional post-RMSNorm, rounded to BF16

@@ -97,6 +97,9 @@ def moe_finalize_rmsnorm(gemm2_permuted: torch.Tensor, expert_weights: torch.Ten
         raise ValueError("output and the index map disagree on num_tokens")
     if nw.shape[0] != os_[1]:
         raise ValueError("norm_weight and output disagree on hidden")
+    if gs[1] < os_[1]:
+        # a narrowed view would otherwise let the kernel read past its columns
+        raise ValueError("gemm2_permuted has fewer columns than output's hidden")
     dev = out.device
     if dev.type != "cuda" or g.device != dev or w.device != dev or idx.device != dev or \
             nw.device != dev:
@@ -168,6 +171,9 @@ def beam_moe_finalize_norm_residual_norm(
     residual) with scales (s0, s1), (1, 1) when None; ``hidden`` may be
     ``residual`` itself.
     """
+    # the C ABI rejects the same combination (MF_ERR_INVALID)
+    _req(normalized is None or next_eps is not None,
+         "normalized is only written by the next norm: pass next_eps with it")
     w, r = expert_weights, residual
     _req(w.dim() == 2 and w.dtype == torch.float32 and w.is_contiguous(),
          "expert_weights must be a contiguous 2-D FP32 tensor")
@@ -190,8 +196,6 @@ def beam_moe_finalize_norm_residual_norm(
         hidden = torch.empty_like(r)
     if normalized is None and next_eps is not None:
         normalized = torch.empty_like(r)
-    if next_eps is None:
-        normalized = None
     for o in (hidden, normalized):
         if o is not None:
             _req(o.shape == r.shape and o.dtype == torch.bfloat16 and o.is_contiguous() and

@@ -163,8 +163,8 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>()) beam_token_cta_kernel
 // f = BF16(v * rs * post_weight) (or v), then hidden = BF16(s0 f + s1 residual)
 // in FP32 (one product, one FMA), stored; with the next norm, normalized =
 // BF16(hidden * rsqrt(mean(hidden^2) + next_eps) * next_weight).  Each thread
-// reads the residual chunks it later overwrites, so hidden may be written into
-// the residual buffer itself.
+// reads the residual chunks it later overwrites (with coherent loads, not the
+// read-only path), so hidden may be written into the residual buffer itself.
 // WARP: one warp holds the whole token (the RMS is a warp reduction, `red`
 // unused); otherwise the CTA does (a shared-memory reduction over NT/32 warps).
 template <int CPT, bool WARP = false>
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
             const int chunk = tid + c * NT;
-            resq[c] = ld_nc_na_16(a.residual + t * H + static_cast<int64_t>(chunk) * kChunkElems);
+            resq[c] = ld_na_16(a.residual + t * H + static_cast<int64_t>(chunk) * kChunkElems);
             nwq[c] = a.next_weight
                          ? __ldg(reinterpret_cast<const uint4 *>(a.next_weight) + chunk)
                          : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(32 * kBeamWarpTokens)
 #pragma unroll
         for (int c = 0; c < CPW; ++c) {
             const int chunk = lane + c * 32;
-            resq[c] = ld_nc_na_16(a.residual + t * H + static_cast<int64_t>(chunk) * kChunkElems);
+            resq[c] = ld_na_16(a.residual + t * H + static_cast<int64_t>(chunk) * kChunkElems);
             nwq[c] = a.next_weight
                          ? __ldg(reinterpret_cast<const uint4 *>(a.next_weight) + chunk)
                          : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);

@@ -61,6 +61,17 @@ __device__ __forceinline__ uint4 ld_nc_na_16(const void *p) {
     return r;
 }
 
+// Coherent 16-byte load that does not allocate in L1: for data this kernel
+// may itself overwrite (the residual op may write hidden into its residual
+// buffer), where the read-only (.nc) path is not allowed.
+__device__ __forceinline__ uint4 ld_na_16(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
 // Streaming 16-byte store (written once, not re-read by this kernel).
 __device__ __forceinline__ void st_cs_16(void *p, const uint4 &v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};"

@@ -210,3 +210,36 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
                                 torch.ones(4096, dtype=torch.bfloat16),
                                 torch.empty((2, 4096), dtype=torch.bfloat16),
                                 eps=1e-6, gain_center=0.0, weight_before_norm=False)
+
+
+def _no_library_call():
+    raise AssertionError("the binding reached the library before rejecting its arguments")
+
+
+def test_binding_rejects_normalized_without_next_eps(monkeypatch):
+    # the C ABI returns MF_ERR_INVALID for a normalized output without the next
+    # norm; the binding raises for the same combination before calling it
+    import torch
+    import moe_finalize_rmsnorm_gb300 as mf
+    monkeypatch.setattr(mf, "lib", _no_library_call)
+    x = torch.zeros((4 * 2, 256), dtype=torch.bfloat16)
+    w = torch.ones((4, 2))
+    r = torch.zeros((3, 256), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="next_eps"):
+        mf.beam_moe_finalize_norm_residual_norm(x, w, r, None, None, None, None, None,
+                                                normalized=torch.empty_like(r))
+
+
+def test_binding_rejects_gemm2_narrower_than_hidden(monkeypatch):
+    # a narrowed view keeps the parent's row stride: without the column check the
+    # row-stride rule alone would let the kernel read columns outside the view
+    import torch
+    import moe_finalize_rmsnorm_gb300 as mf
+    monkeypatch.setattr(mf, "lib", _no_library_call)
+    g = torch.zeros((16, 4096), dtype=torch.bfloat16)[:, :2048]
+    assert g.stride(0) == 4096
+    with pytest.raises(ValueError, match="fewer columns"):
+        mf.moe_finalize_rmsnorm(g, torch.ones((2, 8)), torch.zeros((2, 8), dtype=torch.int32),
+                                torch.ones(4096, dtype=torch.bfloat16),
+                                torch.empty((2, 4096), dtype=torch.bfloat16),
+                                eps=1e-6, gain_center=0.0, weight_before_norm=False)
