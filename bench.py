@@ -179,6 +179,88 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inwin)}
 
 
+class NvmlClock:
+    """Read-only NVML queries of one GPU (SM clock, power draw, clock-event
+    reasons), polled from the host thread while the timed launches run, so a
+    timed region of a few milliseconds still holds samples.  Nothing is set."""
+
+    # nvmlClocksEventReason* bits (nvml.h) of the reasons the record reports
+    REASON_BITS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8),
+                   ("sw_thermal_slowdown", 0x20), ("hw_thermal_slowdown", 0x40))
+    NVML_CLOCK_SM = 1
+
+    def __init__(self, uuid: str | None):
+        import ctypes
+        self.ct = ctypes
+        self.error = None
+        self.max_mhz = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
+            if not uuid:
+                raise OSError("no device UUID")
+            u = "GPU-" + uuid.lower().replace("gpu-", "")
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) != 0:
+                raise OSError(f"no NVML device {u}")
+            self.reasons_fn = (getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                               or lib.nvmlDeviceGetCurrentClocksThrottleReasons)
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.lib, self.h = lib, h
+        except (OSError, AttributeError) as e:
+            self.error = f"NVML unavailable: {e}"
+
+    def sample(self):
+        """(wall time, SM MHz, watts, reason bits) or None."""
+        if self.error:
+            return None
+        c = self.ct
+        clk, mw, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.NVML_CLOCK_SM, c.byref(clk)) != 0:
+            return None
+        self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(mw))
+        self.reasons_fn(self.h, c.byref(rs))
+        return (time.time(), float(clk.value), mw.value / 1000.0, int(rs.value))
+
+    def poll(self, end_event, into: list, interval_s: float = 0.0005) -> None:
+        """Sample until end_event (recorded after the timed launches) completes."""
+        while not end_event.query():
+            smp = self.sample()
+            if smp is None:
+                return
+            into.append(smp)
+            time.sleep(interval_s)
+
+    def summary(self, samples: list) -> dict:
+        if not samples:
+            return {"samples": 0}
+        reasons = sorted({name for _, _, _, bits in samples for name, b in self.REASON_BITS
+                          if bits & b})
+        return {"sm_mhz": statistics.median(s[1] for s in samples), "sm_max_mhz": self.max_mhz,
+                "power_w_max": max(s[2] for s in samples), "reasons": reasons,
+                "samples": len(samples)}
+
+
+def clock_record(smi: dict, nvml: NvmlClock, inwin: list) -> dict:
+    """The line's clock record: NVML samples taken inside the timed region
+    (the host polls while the launches run), with the nvidia-smi background
+    samples as the fallback and for context."""
+    if nvml.error or not inwin:
+        rec = dict(smi)
+        rec["source"] = "nvidia-smi every 50 ms" + (f" ({nvml.error})" if nvml.error else "")
+        return rec
+    rec = nvml.summary(inwin)
+    rec["reasons"] = sorted(set(rec["reasons"]) | set(smi.get("reasons", [])))
+    rec["samples_in_timed_region"] = len(inwin) + smi.get("samples_in_timed_region", 0)
+    rec["samples"] = len(inwin) + smi.get("samples", 0)
+    rec["source"] = ("NVML (read-only) polled by the host while the timed launches ran, "
+                     "plus nvidia-smi every 50 ms")
+    return rec
+
+
 def gpu_uuid(device_index: int) -> str | None:
     import torch
     try:
@@ -438,7 +520,11 @@ def run_reference(args) -> None:
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": desc, "tokens_per_step": sample},
+        # the same keys, with the same meaning, as the GPU arm's config: the
+        # tokens one step finalizes and how the job is laid out
+        "config": {"workload": desc, "global_batch": sample,
+                   "parallelism": "single GPU" if world == 1 else
+                   f"rank 0 of {world} (the other ranks idle)"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{sample} consecutive tokens of the batch per step, "
                                    f"{threads} threads",
@@ -514,7 +600,10 @@ def run_ours(args) -> None:
     if mf.device_status(clear=True) != 0:
         raise SystemExit("device wait timeout during warm-up")
 
-    clocks = ClockSampler(gpu_uuid(local_rank))
+    uuid = gpu_uuid(local_rank)
+    clocks = ClockSampler(uuid)
+    nvml = NvmlClock(uuid)
+    inwin: list = []  # NVML samples taken while the timed launches run
     clocks.start()
     if world > 1:
         dist.barrier()
@@ -535,6 +624,7 @@ def run_ours(args) -> None:
             job.launch(i)
             ev[i][1].record(stream)
         end.record(stream)
+        nvml.poll(end, inwin)
         torch.cuda.synchronize(device)
         t_wall1 = time.time()
         cold_ms = [a.elapsed_time(b) for a, b in ev]
@@ -555,6 +645,7 @@ def run_ours(args) -> None:
         start.record(stream)
         graph.replay()
         end.record(stream)
+        nvml.poll(end, inwin)
         torch.cuda.synchronize(device)
         t_wall1 = time.time()
     else:
@@ -565,6 +656,7 @@ def run_ours(args) -> None:
         for i in range(args.steps):
             job.launch(i)
         end.record(stream)
+        nvml.poll(end, inwin)
         torch.cuda.synchronize(device)
         t_wall1 = time.time()
     if world > 1:
@@ -616,7 +708,7 @@ def run_ours(args) -> None:
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": job.bytes_per_launch},
         "gpu_launches": args.steps,
-        "clocks": clocks.summary(t_wall0, t_wall1),
+        "clocks": clock_record(clocks.summary(t_wall0, t_wall1), nvml, inwin),
         **extra,
     }
 
@@ -626,21 +718,151 @@ def run_ours(args) -> None:
         threads = os.cpu_count() or 1
         T = total_tokens(kind, case)
         n = min(T, args.cpu_tokens)
-        secs = time_oracle(kind, case, 0, n, threads)
+        # passes over the same tokens until about a second of wall time (some
+        # 10-20 s of CPU work on a 16-core host), at most 16
+        secs, passes = time_oracle(kind, case, 0, n, threads), 1
+        while secs < 1.0 and passes < 16:
+            secs += time_oracle(kind, case, 0, n, threads)
+            passes += 1
         n1 = min(n, max(1, n // 8))
         secs1 = time_oracle(kind, case, 0, n1, 1)
-        line["cpu_baseline"] = {"value": n / secs, "unit": "tokens/s", "cores": threads,
+        line["cpu_baseline"] = {"value": n * passes / secs, "unit": "tokens/s", "cores": threads,
                                 "kind": "oracle",
-                                "sample": f"the first {n} tokens of the same batch, one pass, "
-                                          f"{threads} threads ({secs:.2f} s wall)",
+                                "sample": f"the first {n} tokens of the same batch, {passes} "
+                                          f"passes, {threads} threads ({secs:.2f} s wall)",
                                 "single_thread_value": n1 / secs1,
                                 "single_thread_sample": f"the first {n1} tokens, 1 thread",
-                                "host_gbs": n / secs * bytes_per_token(kind, case) / 1e9,
+                                "host_gbs": n * passes / secs * bytes_per_token(kind, case)
+                                / 1e9,
                                 "cpu": host_cpu()}
+    if rank == 0 and world == 1 and args.workload == "roofline" and not (
+            args.cold or args.graph or args.no_other_configs):
+        line["other_configs"] = run_other_configs(torch, mf, device, nvml)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def _timed_back_to_back(torch, job: Job, stream, device, launches: int, nvml: NvmlClock):
+    """Average launch (ms) of `launches` back-to-back launches between one event
+    pair, after five untimed ones; NVML samples taken while they run."""
+    for i in range(5):
+        job.launch(i)
+    torch.cuda.synchronize(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    inwin: list = []
+    start.record(stream)
+    for i in range(launches):
+        job.launch(i)
+    end.record(stream)
+    nvml.poll(end, inwin)
+    torch.cuda.synchronize(device)
+    return start.elapsed_time(end) / launches, inwin
+
+
+def _timed_graph(torch, job: Job, device, launches: int, nvml: NvmlClock):
+    """Average launch (ms) of `launches` launches replayed from one CUDA graph
+    (warm: the inputs stay in L2), after one untimed replay."""
+    for i in range(3):
+        job.launch(i)
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(cap), torch.cuda.graph(graph, stream=cap):
+        for i in range(launches):
+            job.launch(i)
+    torch.cuda.synchronize(device)
+    graph.replay()
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    inwin: list = []
+    start.record(stream)
+    graph.replay()
+    end.record(stream)
+    nvml.poll(end, inwin)
+    torch.cuda.synchronize(device)
+    return start.elapsed_time(end) / launches, inwin
+
+
+def _timed_cold(torch, job: Job, stream, device, launches: int, nvml: NvmlClock, scratch):
+    """Per-launch times (ms) with the L2 flushed before every launch (a write of
+    twice its size, not timed) and an event pair around each launch."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(launches)]
+    end = torch.cuda.Event()
+    inwin: list = []
+    for i in range(launches):
+        scratch.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        job.launch(i)
+        ev[i][1].record(stream)
+    end.record(stream)
+    nvml.poll(end, inwin)
+    torch.cuda.synchronize(device)
+    return [a.elapsed_time(b) for a, b in ev], inwin
+
+
+def run_other_configs(torch, mf, device, nvml: NvmlClock) -> dict:
+    """The other workloads of the path, timed on the same GPU after the
+    headline: finalize of 16 tokens and the decode sizes (warm from one CUDA
+    graph, and cold), finalize of 4096 tokens with padded rows, Beam of 8000
+    live tokens and the residual op (back to back; inputs larger than L2)."""
+    stream = torch.cuda.current_stream(device)
+    peak, _ = measured_peaks()
+    out: dict = {}
+
+    def bandwidth_entry(job, launches, desc):
+        ms, inwin = _timed_back_to_back(torch, job, stream, device, launches, nvml)
+        gbs = job.bytes_per_launch / (ms / 1e3) / 1e9
+        return {"workload": desc, "kernel": job.kernel, "us_per_launch": ms * 1e3,
+                "tokens_per_s": job.units_per_step / (ms / 1e3), "achieved_gbs": gbs,
+                "frac": gbs / peak, "algorithmic_bytes_per_launch": job.bytes_per_launch,
+                "launches": launches,
+                "timing": "one CUDA event pair around the back-to-back launches",
+                "clocks": nvml.summary(inwin)}
+
+    scratch = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def latency_entry(job, desc):
+        warm_ms, win1 = _timed_graph(torch, job, device, 200, nvml)
+        cold, win2 = _timed_cold(torch, job, stream, device, 30, nvml, scratch)
+        return {"workload": desc, "kernel": job.kernel,
+                "warm_us_per_launch": warm_ms * 1e3,
+                "warm_timing": "200 launches replayed from one CUDA graph, inputs in L2",
+                "cold_us_p10_p50_p90": [float(np.percentile(cold, q)) * 1e3 for q in (10, 50, 90)],
+                "cold_timing": (f"L2 flushed before each of 30 launches ({L2_FLUSH_BYTES / 1e6:.0f}"
+                                " MB scratch write, not timed), an event pair around each"),
+                "algorithmic_bytes_per_launch": job.bytes_per_launch,
+                "clocks": nvml.summary(win1 + win2)}
+
+    kind, case, desc = workload_case("small", None, 0)
+    out["finalize_T16"] = latency_entry(make_tp_job(torch, mf, case, device, "auto", False), desc)
+    for T in si.DECODE_TOKENS:
+        kind, case, desc = workload_case("decode", T, 0)
+        out[f"decode_T{T}"] = latency_entry(make_tp_job(torch, mf, case, device, "auto", False),
+                                            desc)
+    del scratch
+
+    kind, case, desc = workload_case("padded", None, 0)
+    job = make_tp_job(torch, mf, case, device, "auto", False)
+    out["finalize_T4096_stride4160"] = bandwidth_entry(job, 500, desc)
+    del job
+
+    kind, case, desc = workload_case("beam", None, 0)
+    job = make_beam_job(torch, mf, case, device, "auto")
+    out["beam_live8000"] = bandwidth_entry(job, 200, desc)
+    del job
+    kind, case, desc = workload_case("beam_residual", None, 0)
+    job = make_beam_residual_job(torch, mf, case, device)
+    out["beam_residual_live8000"] = bandwidth_entry(job, 200, desc)
+    del job
+    torch.cuda.synchronize(device)
+    if mf.device_status(clear=True) != 0:
+        raise SystemExit("device wait timeout while timing the other workloads")
+    return out
 
 
 def run_e2e(torch, mf, job: Job, kind: str, case, device, steps: int) -> dict:
@@ -747,6 +969,8 @@ def parse_args(argv=None):
     p.add_argument("--e2e-steps", type=int, default=8)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-other-configs", action="store_true",
+                   help="skip the other workloads timed after the headline (default run only)")
     p.add_argument("--cpu-tokens", type=int, default=32768,
                    help="tokens of the batch the CPU oracle baseline processes")
     a = p.parse_args(argv)

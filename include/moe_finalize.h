@@ -37,7 +37,11 @@
  *     output may be its residual buffer).
  *   - Kernel waits are bounded (about two seconds of wall time); a wait that
  *     gives up sets MF_ERR_DEVICE_TIMEOUT in the device status word, which
- *     mf_device_status() reads.
+ *     mf_device_status() reads.  After such a timeout the outputs of that call
+ *     and of any later kernel on the context are unspecified: the CTA that
+ *     gave up waits once more (also bounded) for its copies in flight, but if
+ *     that wait gives up too, a bulk copy may still land in shared memory that
+ *     another CTA then uses.  Discard the results and the CUDA context.
  *   - The first call on a device sets kernel attributes; make it before any
  *     CUDA graph capture.  Captured calls replay with their arguments baked in.
  */

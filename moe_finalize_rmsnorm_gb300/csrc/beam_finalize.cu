@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
                 if (!mbar_wait(b, phase, a.timeout_ns)) {
                     atomicOr(a.status, kStatusWaitTimeout);
                     ok = false;
-                    (void)mbar_wait(b, phase, a.timeout_ns);  // let the copy land before exit
+                    (void)mbar_wait(b, phase, a.timeout_ns);  // bounded: the copy may land, or not, before exit
                 }
             }
             const float w = wsm[k0 + r];
@@ -424,7 +424,7 @@ __global__ void __launch_bounds__(32 * kBeamWarpTokens)
         if (!mbar_wait(bar, phase, a.timeout_ns)) {
             atomicOr(a.status, kStatusWaitTimeout);
             ok = false;
-            (void)mbar_wait(bar, phase, a.timeout_ns);  // let the copy land before exit
+            (void)mbar_wait(bar, phase, a.timeout_ns);  // bounded: the copy may land, or not, before exit
         }
         for (int r = 0; r < n; ++r) {
             const float w = __shfl_sync(0xffffffffu, wl, k0 + r);

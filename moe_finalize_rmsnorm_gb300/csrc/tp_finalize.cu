@@ -42,7 +42,11 @@
 // routed_moe, topk_ids parameter), whose low half is the weight.
 //
 // Every wait on an mbarrier is bounded (TpArgs::timeout_ns); a wait that gives
-// up ORs kStatusWaitTimeout into the device status word and the kernel returns.
+// up ORs kStatusWaitTimeout into the device status word, waits once more (also
+// bounded) for the copies it issued, and the kernel returns without storing.
+// If that second wait gives up too, a copy may still be writing into shared
+// memory after the CTA has left, so after a timeout the outputs of the call and
+// of later kernels on the context are unspecified.
 
 #include "common.cuh"
 #include "kernels.h"
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kBulkThreads)
         if (!mbar_wait(b, 0u, a.timeout_ns)) {
             atomicOr(a.status, kStatusWaitTimeout);
             ok = false;
-            (void)mbar_wait(b, 0u, a.timeout_ns);  // let the copy land before exit
+            (void)mbar_wait(b, 0u, a.timeout_ns);  // bounded: the copy may land, or not, before exit
         }
         uint4 q[CPT];
 #pragma unroll
@@ -480,7 +484,7 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
                 if (!mbar_wait(b, phase, a.timeout_ns)) {
                     atomicOr(a.status, kStatusWaitTimeout);
                     ok = false;
-                    (void)mbar_wait(b, phase, a.timeout_ns);  // let the copies land before exit
+                    (void)mbar_wait(b, phase, a.timeout_ns);  // bounded: the copies may land, or not, before exit
                 }
             }
             const float w = w_s[order_s[p0 + r]];
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(32 * warp_tokens_per_cta<CPW>())
         if (!mbar_wait(bar, phase, a.timeout_ns)) {
             atomicOr(a.status, kStatusWaitTimeout);
             ok = false;
-            (void)mbar_wait(bar, phase, a.timeout_ns);  // let the copies land before exit
+            (void)mbar_wait(bar, phase, a.timeout_ns);  // bounded: the copies may land, or not, before exit
         }
         for (int r = 0; r < n; ++r) {
             const int k = __ffs(rest) - 1;

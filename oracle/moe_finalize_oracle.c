@@ -31,7 +31,9 @@
  * reduction runs in float with slots in ascending order, one fused
  * multiply-add (C99 fmaf, single rounding) per slot.  The pages fix no
  * precision for the normalisation, so it runs in double (float64), and the
- * result is rounded once from double to BF16, round-to-nearest-even.  For the
+ * result is rounded once from double to BF16, round-to-nearest-even.  That
+ * includes the pre-norm gain product of weight_before_norm, acc * g, which is
+ * formed in double from the two FP32 values (exact there: no extra rounding).  For the
  * Beam scale, which the docstring applies to the expert reduction once it has
  * been rounded to BF16, the product is read as PyTorch's BF16 tensor times a
  * scalar: an FP32 product rounded to BF16.

@@ -123,3 +123,51 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["steps"] == 3 and d["warmup"] == 3
+    # the config carries the GPU arm's keys with the same meaning: the whole
+    # 16-token batch fits the time budget, so one step finalizes all of it
+    assert d["config"]["global_batch"] == 16 and d["config"]["parallelism"] == "single GPU"
+    assert set(d["config"]) == {"workload", "global_batch", "parallelism"}
+
+
+def _fake_nvml(max_mhz=2070.0):
+    n = bench.NvmlClock.__new__(bench.NvmlClock)
+    n.error, n.max_mhz = None, max_mhz
+    return n
+
+
+def test_nvml_summary_decodes_the_reason_bits():
+    n = _fake_nvml()
+    s = n.summary([(1.0, 2070.0, 900.0, 0x0), (1.1, 1995.0, 1380.0, 0x4 | 0x1),
+                   (1.2, 2070.0, 950.0, 0x0)])
+    assert s["sm_mhz"] == 2070.0 and s["sm_max_mhz"] == 2070.0 and s["power_w_max"] == 1380.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 3     # idle bit 0x1 not a reason
+    s = n.summary([(1.0, 1200.0, 900.0, 0x8 | 0x40 | 0x20)])
+    assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+
+
+def test_clock_record_counts_samples_inside_the_timed_region():
+    smi = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 1,
+           "samples_in_timed_region": 0}
+    rec = bench.clock_record(smi, _fake_nvml(), [(1.0, 2055.0, 800.0, 0), (1.001, 2070.0, 820.0, 0)])
+    assert rec["samples_in_timed_region"] == 2 and rec["sm_mhz"] == 2062.5
+    assert rec["samples"] == 3 and "NVML" in rec["source"]
+    # without NVML the nvidia-smi record stands, and says so
+    broken = _fake_nvml()
+    broken.error = "NVML unavailable: test"
+    rec = bench.clock_record(smi, broken, [])
+    assert rec["samples_in_timed_region"] == 0 and "nvidia-smi" in rec["source"]
+
+
+def test_nvml_poll_stops_when_the_region_ends():
+    class Ev:
+        def __init__(self):
+            self.n = 0
+
+        def query(self):
+            self.n += 1
+            return self.n > 3
+    n = _fake_nvml()
+    n.sample = lambda: (0.0, 2070.0, 500.0, 0)
+    got = []
+    n.poll(Ev(), got, interval_s=0.0)
+    assert len(got) == 3
