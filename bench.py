@@ -820,7 +820,7 @@ def run_other_configs(torch, mf, device, nvml: NvmlClock) -> dict:
         return {"workload": desc, "kernel": job.kernel, "us_per_launch": ms * 1e3,
                 "tokens_per_s": job.units_per_step / (ms / 1e3), "achieved_gbs": gbs,
                 "frac": gbs / peak, "algorithmic_bytes_per_launch": job.bytes_per_launch,
-                "launches": launches,
+                "traffic": recorded_traffic(job.kernel, job.name), "launches": launches,
                 "timing": "one CUDA event pair around the back-to-back launches",
                 "clocks": nvml.summary(inwin)}
 
