@@ -538,7 +538,7 @@ def run_reference(args) -> None:
 # ---------------------------------------------------------------------------
 # the CUDA path
 
-def per_launch_pass(torch, job: Job, stream, n: int, alternating: bool) -> dict:
+def per_launch_pass(torch, launch, stream, n: int, alternating: bool) -> dict:
     """Distribution of single-launch times, from a pass after the timed region
     with an event pair around every launch.  The event records between
     launches make each launch wait for the one before it to drain and expose
@@ -548,7 +548,7 @@ def per_launch_pass(torch, job: Job, stream, n: int, alternating: bool) -> dict:
           for _ in range(n)]
     for i in range(n):
         ev[i][0].record(stream)
-        job.launch(i)
+        launch(i)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b) for a, b in ev]
@@ -592,10 +592,22 @@ def run_ours(args) -> None:
     else:
         job = make_beam_job(torch, mf, case, device, args.variant)
     stream = torch.cuda.current_stream(device)
+    # inputs of a few L2 sizes only: rotate among copies so that no launch finds
+    # the previous launch's rows in L2 (one copy for the default workload)
+    n_copies = 1 if (args.cold or args.graph) else input_copies(job.bytes_per_launch)
+    sets = [tuple(job.device_tensors)] + [
+        tuple(None if t is None else _same_layout_copy(torch, t) for t in job.device_tensors)
+        for _ in range(n_copies - 1)]
+
+    def launch(i):
+        if n_copies == 1:
+            job.launch(i)
+        else:
+            job.launch(i, tensors=sets[i % n_copies])
 
     # warm-up
     for i in range(args.warmup):
-        job.launch(i)
+        launch(i)
     torch.cuda.synchronize(device)
     if mf.device_status(clear=True) != 0:
         raise SystemExit("device wait timeout during warm-up")
@@ -654,7 +666,7 @@ def run_ours(args) -> None:
         t_wall0 = time.time()
         start.record(stream)
         for i in range(args.steps):
-            job.launch(i)
+            launch(i)
         end.record(stream)
         nvml.poll(end, inwin)
         torch.cuda.synchronize(device)
@@ -679,7 +691,7 @@ def run_ours(args) -> None:
         extra["cold_launch_us_p10_p50_p90"] = [float(np.percentile(cold_ms, q)) * 1e3
                                                for q in (10, 50, 90)]
     elif not args.graph:
-        extra["per_launch_events"] = per_launch_pass(torch, job, stream, min(args.steps, 400),
+        extra["per_launch_events"] = per_launch_pass(torch, launch, stream, min(args.steps, 400),
                                                      args.workload == "roofline")
         if mf.device_status(clear=True) != 0:
             raise SystemExit("device wait timeout in the per-launch pass")
@@ -692,9 +704,13 @@ def run_ours(args) -> None:
         "config": {"workload": desc, "global_batch": job.units_per_step * world,
                    "l2": (f"flushed before every launch ({L2_FLUSH_BYTES / 1e6:.0f} MB scratch "
                           "write, not timed)") if args.cold else
+                         (f"{n_copies} copies of the inputs, launch i reads copy i mod "
+                          f"{n_copies}: each launch's rows were last read at least 4 x L2 of "
+                          "traffic earlier") if n_copies > 1 else
                          ("no flush: every step reads its inputs from HBM "
                           f"({job.bytes_per_launch / 1e9:.3f} GB per launch, L2 is 0.13 GB)"
-                          if job.bytes_per_launch > 256e6 else "inputs smaller than L2 (warm)"),
+                          if job.bytes_per_launch >= 4 * L2_BYTES else
+                          "inputs smaller than L2 (warm)"),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "timing": "one CUDA graph of all timed launches" if args.graph
                    else ("an event pair around each launch, summed" if args.cold
@@ -744,17 +760,48 @@ def run_ours(args) -> None:
         dist.destroy_process_group()
 
 
-def _timed_back_to_back(torch, job: Job, stream, device, launches: int, nvml: NvmlClock):
+# GB300's L2; a launch's inputs count as cold when the launches since their
+# last use have moved at least four times this much.
+L2_BYTES = 129 * 10 ** 6
+
+
+def input_copies(bytes_per_launch: int) -> int:
+    """Copies of a workload's device buffers to rotate through, so that each
+    launch's rows were last read at least 4 x L2 of traffic ago (1: a single
+    launch already moves that much)."""
+    b = max(int(bytes_per_launch), 1)
+    if b >= 4 * L2_BYTES or b < L2_BYTES:  # cold by size, or warm by design (decode sizes)
+        return 1
+    return 1 + -(-4 * L2_BYTES // b)
+
+
+def _same_layout_copy(torch, t):
+    """A copy with the same strides (a padded row stride stays padded)."""
+    c = torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device=t.device)
+    return c.copy_(t)
+
+
+def _timed_back_to_back(torch, job: Job, stream, device, launches: int, nvml: NvmlClock,
+                        sets=None):
     """Average launch (ms) of `launches` back-to-back launches between one event
-    pair, after five untimed ones; NVML samples taken while they run."""
+    pair, after five untimed ones; NVML samples taken while they run.  With
+    `sets` (copies of the job's device buffers) launch i uses copy i mod n."""
+    sets = sets or [None]
+
+    def go(i):
+        t = sets[i % len(sets)]
+        if t is None:
+            job.launch(i)
+        else:
+            job.launch(i, tensors=t)
     for i in range(5):
-        job.launch(i)
+        go(i)
     torch.cuda.synchronize(device)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     inwin: list = []
     start.record(stream)
     for i in range(launches):
-        job.launch(i)
+        go(i)
     end.record(stream)
     nvml.poll(end, inwin)
     torch.cuda.synchronize(device)
@@ -815,13 +862,24 @@ def run_other_configs(torch, mf, device, nvml: NvmlClock) -> dict:
     out: dict = {}
 
     def bandwidth_entry(job, launches, desc):
-        ms, inwin = _timed_back_to_back(torch, job, stream, device, launches, nvml)
+        # consecutive launches read different copies of the inputs: a workload of
+        # a few L2 sizes would otherwise find part of its rows still in L2
+        n = input_copies(job.bytes_per_launch)
+        sets = [tuple(job.device_tensors)] + [
+            tuple(None if t is None else _same_layout_copy(torch, t) for t in job.device_tensors)
+            for _ in range(n - 1)]
+        ms, inwin = _timed_back_to_back(torch, job, stream, device, launches, nvml, sets)
+        del sets
         gbs = job.bytes_per_launch / (ms / 1e3) / 1e9
         return {"workload": desc, "kernel": job.kernel, "us_per_launch": ms * 1e3,
                 "tokens_per_s": job.units_per_step / (ms / 1e3), "achieved_gbs": gbs,
                 "frac": gbs / peak, "algorithmic_bytes_per_launch": job.bytes_per_launch,
                 "traffic": recorded_traffic(job.kernel, job.name), "launches": launches,
                 "timing": "one CUDA event pair around the back-to-back launches",
+                "l2": (f"{n} copies of the inputs, launch i reads copy i mod {n}: each launch's "
+                       "rows were last read at least 4 x L2 of traffic earlier") if n > 1 else
+                      ("no flush: every launch reads its inputs from HBM "
+                       f"({job.bytes_per_launch / 1e9:.3f} GB per launch, L2 is 0.13 GB)"),
                 "clocks": nvml.summary(inwin)}
 
     scratch = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)

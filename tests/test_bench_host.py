@@ -171,3 +171,22 @@ def test_nvml_poll_stops_when_the_region_ends():
     got = []
     n.poll(Ev(), got, interval_s=0.0)
     assert len(got) == 3
+
+
+def test_input_copies_keep_each_launch_cold():
+    # a launch of a few L2 sizes rotates among copies so that its rows were last
+    # read at least 4 x L2 of traffic earlier; large launches and L2-sized
+    # (decode) ones use their buffers as they are
+    L2 = bench.L2_BYTES
+    for b in (L2, 302186496, 2 * L2, 4 * L2 - 1):
+        n = bench.input_copies(b)
+        assert n > 1 and (n - 1) * b >= 4 * L2
+    assert bench.input_copies(2418016256) == 1 and bench.input_copies(4 * L2) == 1
+    assert bench.input_copies(73792) == 1 and bench.input_copies(L2 - 1) == 1
+
+
+def test_same_layout_copy_keeps_a_padded_row_stride():
+    import torch
+    t = torch.arange(6 * 4160, dtype=torch.float32).view(6, 4160)[:, :4096]
+    c = bench._same_layout_copy(torch, t)
+    assert c.stride() == (4160, 1) and torch.equal(c, t) and c.data_ptr() != t.data_ptr()
