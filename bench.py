@@ -308,10 +308,7 @@ def make_tp_job(torch, mf, case: si.TpCase, device, variant: str, alternate: boo
 
     chosen = (mf.select_finalize_variant(T, case.hidden, case.top_k) if variant == "auto"
               else variant)
-    kernel = {"bulk": "tp_token_bulk_kernel", "token_cta": "tp_token_cta_kernel",
-              "cluster": "tp_cluster_kernel"}[chosen]
-    if (case.hidden, case.top_k) != (4096, 8):
-        kernel = "tp_warp_bulk_kernel" if case.hidden <= 1024 else "tp_generic_bulk_kernel"
+    kernel = mf.finalize_kernel_name(T, case.hidden, case.top_k, variant)
     job = Job(case.name, T, si.algorithmic_bytes_tp(T, case.hidden, case.top_k, wbytes), kernel,
               launch, case, {"variant": chosen})
     job.device_tensors = (g, w, idx, nw, out)
@@ -330,9 +327,7 @@ def make_beam_job(torch, mf, case: si.BeamCase, device, variant: str) -> Job:
         mf.beam_moe_finalize(xx, ww, oo, case.routed_scale, pp, case.post_eps, variant=variant)
 
     chosen = mf.select_beam_variant(case.live_tokens, K, H) if variant == "auto" else variant
-    kernel = {"bulk": "beam_token_bulk_kernel", "token_cta": "beam_token_cta_kernel"}[chosen]
-    if chosen == "bulk" and H <= 1024:
-        kernel = "beam_warp_bulk_kernel"
+    kernel = mf.beam_kernel_name(case.live_tokens, K, H, variant)
     job = Job(case.name, case.live_tokens, si.algorithmic_bytes_beam(case.live_tokens, H, K),
               kernel, launch, case, {"variant": chosen})
     job.device_tensors = (x, w, pw, out)
@@ -357,7 +352,8 @@ def make_beam_residual_job(torch, mf, case: si.BeamCase, device) -> Job:
                                                 case.routed_scale, hidden=hh, normalized=oo)
 
     job = Job(case.name + "_residual", T, si.algorithmic_bytes_beam_residual(T, H, K, True),
-              "beam_token_bulk_kernel", launch, case, {"variant": "bulk"})
+              mf.beam_kernel_name(T, K, H, "auto", residual=True), launch, case,
+              {"variant": "bulk"})
     job.device_tensors = (x, w, res, pw, nw, hid, nrm)
     job.n_outputs = 2
     return job

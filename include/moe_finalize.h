@@ -254,6 +254,23 @@ mf_variant mf_select_finalize_variant(int64_t num_tokens, int32_t hidden, int32_
 /* The kernel AUTO would run for beam_moe_finalize. */
 mf_variant mf_select_beam_variant(int64_t live_tokens, int32_t top_k, int32_t hidden);
 
+/* Name of the CUDA kernel that moe_finalize_rmsnorm_variant would launch for
+ * these sizes and this variant on the calling thread's current device, for
+ * diagnostics and for matching a profiler's launch list: "tp_cluster_kernel",
+ * "tp_token_cta_kernel", "tp_token_bulk_kernel", "tp_token_bulk_multi_kernel"
+ * (the staged kernel with several tokens per CTA, from five waves of tokens
+ * up), "tp_generic_bulk_kernel" or "tp_warp_bulk_kernel".  The empty string
+ * when nothing would launch (no tokens, unsupported sizes, a variant that does
+ * not apply).  Static string. */
+const char *mf_finalize_kernel_name(int64_t num_tokens, int32_t hidden, int32_t top_k,
+                                    mf_variant variant);
+
+/* The same for beam_moe_finalize_variant, and with nonzero `residual` for
+ * beam_moe_finalize_norm_residual_norm: "beam_token_bulk_kernel",
+ * "beam_warp_bulk_kernel" (hidden 256..1024) or "beam_token_cta_kernel". */
+const char *mf_beam_kernel_name(int64_t live_tokens, int32_t top_k, int32_t hidden,
+                                mf_variant variant, int residual);
+
 /* Human-readable name of a status code (static string). */
 const char *mf_status_string(mf_status status);
 

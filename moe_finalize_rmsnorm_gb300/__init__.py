@@ -25,6 +25,7 @@ __all__ = [
     "moe_finalize_rmsnorm", "tp_moe_finalize_rmsnorm", "beam_moe_finalize",
     "beam_moe_finalize_norm_residual_norm", "MoeFinalizeError",
     "device_status", "selftest_wait_timeout", "select_finalize_variant", "select_beam_variant",
+    "finalize_kernel_name", "beam_kernel_name",
     "version", "set_programmatic_launch", "programmatic_launch", "HIDDEN", "TOP_K",
 ]
 
@@ -221,6 +222,22 @@ def select_finalize_variant(num_tokens: int, hidden: int = HIDDEN, top_k: int = 
 
 def select_beam_variant(live_tokens: int, top_k: int, hidden: int) -> str:
     return VARIANT_NAMES[lib().mf_select_beam_variant(int(live_tokens), int(top_k), int(hidden))]
+
+
+def finalize_kernel_name(num_tokens: int, hidden: int = HIDDEN, top_k: int = TOP_K,
+                         variant: str = "auto") -> str:
+    """Name of the CUDA kernel a moe_finalize_rmsnorm call of these sizes launches
+    on the current device ("" if none would)."""
+    return lib().mf_finalize_kernel_name(int(num_tokens), int(hidden), int(top_k),
+                                         _variant(variant)).decode()
+
+
+def beam_kernel_name(live_tokens: int, top_k: int, hidden: int, variant: str = "auto",
+                     residual: bool = False) -> str:
+    """Name of the CUDA kernel a beam_moe_finalize call (or, with ``residual``,
+    beam_moe_finalize_norm_residual_norm) of these sizes launches."""
+    return lib().mf_beam_kernel_name(int(live_tokens), int(top_k), int(hidden), _variant(variant),
+                                     int(bool(residual))).decode()
 
 
 def device_status(clear: bool = True) -> int:

@@ -34,6 +34,8 @@ SIGNATURES = {
                _int, _f32, _f32, _vp, _vp, _vp]),
     "mf_select_finalize_variant": (_int, [_i64, _i32, _i32]),
     "mf_select_beam_variant": (_int, [_i64, _i32, _i32]),
+    "mf_finalize_kernel_name": (ctypes.c_char_p, [_i64, _i32, _i32, _int]),
+    "mf_beam_kernel_name": (ctypes.c_char_p, [_i64, _i32, _i32, _int, _int]),
     "mf_status_string": (ctypes.c_char_p, [_int]),
     "mf_device_status": (_int, [_int]),
     "mf_selftest_wait_timeout": (_int, [_u64, _vp]),

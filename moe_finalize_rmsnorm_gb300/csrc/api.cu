@@ -183,7 +183,8 @@ mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
     switch (variant) {
         case MF_VARIANT_CLUSTER: return from_launch(mf::launch_tp_cluster(a, wk, s));
         case MF_VARIANT_TOKEN_CTA: return from_launch(mf::launch_tp_token_cta(a, wk, s));
-        case MF_VARIANT_BULK: return from_launch(mf::launch_tp_bulk(a, wk, s));
+        case MF_VARIANT_BULK:
+            return from_launch(mf::launch_tp_bulk(a, wk, d->bulk_per_sm * d->num_sms, s));
         default: return MF_ERR_INVALID;
     }
 }
@@ -319,6 +320,39 @@ mf_variant mf_select_finalize_variant(int64_t num_tokens, int32_t hidden, int32_
     if (hidden < 256 || hidden > 8192 || hidden % 256 != 0 || top_k < 1 || top_k > 32)
         return MF_VARIANT_AUTO;
     return MF_VARIANT_BULK;
+}
+
+const char *mf_finalize_kernel_name(int64_t num_tokens, int32_t hidden, int32_t top_k,
+                                    mf_variant variant) {
+    if (num_tokens <= 0 || variant < MF_VARIANT_AUTO || variant > MF_VARIANT_CLUSTER) return "";
+    if (hidden != mf::kTpHidden || top_k != mf::kTpTopK) {
+        if (hidden < 256 || hidden > 8192 || hidden % 256 != 0 || top_k < 1 || top_k > 32) return "";
+        if (variant != MF_VARIANT_AUTO && variant != MF_VARIANT_BULK) return "";
+        return hidden <= 1024 ? "tp_warp_bulk_kernel" : "tp_generic_bulk_kernel";
+    }
+    const DeviceInfo *d = nullptr;
+    if (device_info(&d) != MF_OK) d = nullptr;
+    if (variant == MF_VARIANT_AUTO) variant = pick_tp(num_tokens, d);
+    switch (variant) {
+        case MF_VARIANT_CLUSTER: return "tp_cluster_kernel";
+        case MF_VARIANT_TOKEN_CTA: return "tp_token_cta_kernel";
+        case MF_VARIANT_BULK:
+            return d != nullptr && mf::tp_bulk_groups(num_tokens, int64_t{d->bulk_per_sm} * d->num_sms) > 0
+                       ? "tp_token_bulk_multi_kernel"
+                       : "tp_token_bulk_kernel";
+        default: return "";
+    }
+}
+
+const char *mf_beam_kernel_name(int64_t live_tokens, int32_t top_k, int32_t hidden,
+                                mf_variant variant, int residual) {
+    if (live_tokens <= 0 || top_k < 1 || top_k > 32 || hidden < 256 || hidden > 8192 ||
+        hidden % 256 != 0)
+        return "";
+    if (variant == MF_VARIANT_AUTO || residual) variant = MF_VARIANT_BULK;
+    if (variant == MF_VARIANT_TOKEN_CTA) return "beam_token_cta_kernel";
+    if (variant != MF_VARIANT_BULK) return "";
+    return hidden <= 1024 ? "beam_warp_bulk_kernel" : "beam_token_bulk_kernel";
 }
 
 mf_variant mf_select_beam_variant(int64_t live_tokens, int32_t top_k, int32_t hidden) {

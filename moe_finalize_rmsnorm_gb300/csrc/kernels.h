@@ -64,15 +64,21 @@ struct BeamArgs {
 // device's opt-in shared memory per block, `smem_per_sm` its shared memory
 // per multiprocessor.
 cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm);
-// CTAs per SM of the staged (bulk) and register (token_cta) hidden-4096 kernels,
-// from the occupancy calculator (after prepare_tp_kernels).
+// CTAs per SM of the staged (bulk; the smaller of its one- and multi-token
+// kernels) and register (token_cta) hidden-4096 kernels, from the occupancy
+// calculator (after prepare_tp_kernels).
 cudaError_t tp_blocks_per_sm(int *bulk, int *token_cta);
 cudaError_t prepare_beam_kernels(int smem_per_sm);
 
 // Hidden 4096, top-k 8.
 cudaError_t launch_tp_token_cta(const TpArgs &a, int weight_kind, cudaStream_t s);
 cudaError_t launch_tp_cluster(const TpArgs &a, int weight_kind, cudaStream_t s);
-cudaError_t launch_tp_bulk(const TpArgs &a, int weight_kind, cudaStream_t s);
+// `resident_ctas`: CTAs of the staged kernel resident at once on the device
+// (CTAs per SM times SMs); it sets how many tokens run in multi-token CTAs.
+cudaError_t launch_tp_bulk(const TpArgs &a, int weight_kind, int resident_ctas, cudaStream_t s);
+// Multi-token CTAs of the staged hidden-4096 kernel for a launch (0: one token
+// per CTA throughout).
+int64_t tp_bulk_groups(int64_t num_tokens, int64_t resident_ctas);
 // Any hidden in 256..8192 (multiple of 256) and top-k in 1..32.
 cudaError_t launch_tp_generic(const TpArgs &a, int weight_kind, int smem_per_sm, cudaStream_t s);
 

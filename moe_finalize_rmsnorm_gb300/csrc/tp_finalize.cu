@@ -350,6 +350,135 @@ __global__ void __launch_bounds__(kBulkThreads)
     if (ok) scale_store<CPT, NT>(acc, g, before, r, a.out + t * kTpHidden, tid);
 }
 
+// The same staged kernel for launches of five waves and more, with several
+// tokens in each of the first `groups` CTAs.  CTA b < groups takes
+// kBulkTokensPerCta consecutive tokens, the CTAs after it one token each (the
+// last waves of the launch).  A CTA with more tokens loads the next token's
+// route while the current token's rows land, and once every thread has read
+// those rows it puts the next token's rows in flight into the same buffer
+// before the current token's norm and stores, so the route's DRAM round trip
+// and the epilogue of all but its last token overlap row traffic.  One-token
+// CTAs at the end keep the drain of a launch as short as with one token per
+// CTA.  Each token's arithmetic is that of tp_token_bulk_kernel: the same bits.
+constexpr int kBulkTokensPerCta = 3;
+constexpr int kBulkSingleWaves = 2;  // waves of one-token CTAs at the end
+
+template <int WK>
+__global__ void __launch_bounds__(kBulkThreads, 3)
+    tp_token_bulk_multi_kernel(const TpArgs a, const int64_t groups) {
+    constexpr int NT = kBulkThreads, NW = NT / 32, CPT = kBulkCPT;
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    __shared__ uint64_t bars[8];
+    __shared__ float red[2][NW];
+
+    const int64_t b = blockIdx.x;
+    const bool grouped = b < groups;
+    int64_t t = grouped ? kBulkTokensPerCta * b : (kBulkTokensPerCta - 1) * groups + b;
+    const int ntok = grouped ? kBulkTokensPerCta : 1;
+    const int tid = threadIdx.x;
+    const uint32_t rows_base = smem_u32(rows_smem);
+
+    pdl_wait();
+    int idx[8];
+    float w[8];
+    load_route<WK>(a, t, idx, w);
+    uint32_t mask = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mask |= (slot_valid(idx[k], a.rows) ? 1u : 0u) << k;
+
+    // one mbarrier per row: the reduction starts on a row as soon as it lands
+    // (thread 0 initialises the barriers and arms them, in its own order)
+    auto issue = [&](const int (&ix)[8], uint32_t m) {
+        const uint64_t policy = policy_evict_first();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if ((m >> k) & 1u) {
+                const uint32_t bb = smem_u32(&bars[k]);
+                mbar_arrive_expect_tx(bb, kTpRowBytes);
+                bulk_copy_g2s_hint(rows_base + k * kTpRowBytes,
+                                   a.gemm2 + static_cast<int64_t>(ix[k]) * a.ld, kTpRowBytes, bb,
+                                   policy);
+            }
+    };
+    if (tid == 0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mbar_init(smem_u32(&bars[k]), 1);
+        fence_mbar_init();
+        issue(idx, mask);
+    }
+    float g[CPT][8];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) load_gain(a, tid + c * NT, g[c]);
+    __syncthreads();  // the barriers are initialised before anyone waits on them
+
+    const bool before = a.before != 0;
+    uint32_t parity = 0;  // bit k: the phase of bars[k] the next wait is for
+    for (int j = 0; j < ntok; ++j, ++t) {
+        int nidx[8];
+        float nw[8];
+        uint32_t nmask = 0;
+        if (j + 1 < ntok) {  // the next token's route, while this token's rows land
+            load_route<WK>(a, t + 1, nidx, nw);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) nmask |= (slot_valid(nidx[k], a.rows) ? 1u : 0u) << k;
+        }
+        float acc[CPT][8];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[c][e] = 0.f;
+        bool ok = true;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (!((mask >> k) & 1u)) continue;
+            const uint32_t bb = smem_u32(&bars[k]);
+            const uint32_t ph = (parity >> k) & 1u;
+            if (!mbar_wait(bb, ph, a.timeout_ns)) {
+                atomicOr(a.status, kStatusWaitTimeout);
+                ok = false;
+                (void)mbar_wait(bb, ph, a.timeout_ns);  // bounded: the copy may land, or not, before exit
+            }
+            uint4 q[CPT];
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) q[c] = lds_16(rows_base + k * kTpRowBytes + (tid + c * NT) * kChunkBytes);
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) {
+                float x[8];
+                unpack8(q[c], x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[c][e] = __fmaf_rn(w[k], x[e], acc[c][e]);
+            }
+        }
+        parity ^= mask;  // the barriers armed for this token moved to their next phase
+        bool more = false;
+        if (j + 1 < ntok) {
+            // every thread has read the buffer, and none gave up waiting: the
+            // next token's rows go in flight before this token's epilogue
+            more = !__syncthreads_or(!ok);
+            if (more && tid == 0) {
+                fence_proxy_async_smem();  // the reads above come before the copies
+                issue(nidx, nmask);
+            }
+        }
+        float *rd = red[j & 1];  // alternate: a slow warp may still read the last one
+        const float ss = warp_sum(prenorm<CPT>(acc, g, before));
+        if ((tid & 31) == 0) rd[tid >> 5] = ss;
+        __syncthreads();
+        float tot = 0.f;
+#pragma unroll
+        for (int i = 0; i < NW; ++i) tot += rd[i];
+        const float r = rsqrtf(__fmaf_rn(tot, 1.0f / kTpHidden, a.eps));
+        if (ok) scale_store<CPT, NT>(acc, g, before, r, a.out + t * kTpHidden, tid);
+        if (!more) break;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            idx[k] = nidx[k];
+            w[k] = nw[k];
+        }
+        mask = nmask;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // any hidden / top-k: one CTA per token, valid rows staged in pieces
 
@@ -660,6 +789,9 @@ cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm) {
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightBF16>, kBulkSmem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightFP32>, kBulkSmem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_kernel<kWeightPacked>, kBulkSmem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_multi_kernel<kWeightBF16>, kBulkSmem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_multi_kernel<kWeightFP32>, kBulkSmem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_multi_kernel<kWeightPacked>, kBulkSmem);
     constexpr int warp_smem1 = kWarpSliceBytes * warp_tokens_per_cta<1>();
     constexpr int warp_smem = kWarpSliceBytes * warp_tokens_per_cta<2>();  // CPW 2..4
     if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<1, kWeightBF16>, warp_smem1);
@@ -687,8 +819,13 @@ cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm) {
 }
 
 cudaError_t tp_blocks_per_sm(int *bulk, int *token_cta) {
+    int multi = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         bulk, tp_token_bulk_kernel<kWeightFP32>, kBulkThreads, kBulkSmem);
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &multi, tp_token_bulk_multi_kernel<kWeightFP32>, kBulkThreads, kBulkSmem);
+    if (e == cudaSuccess && multi < *bulk) *bulk = multi;  // both kernels' waves: the smaller
     if (e == cudaSuccess)
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(token_cta, tp_token_cta_kernel<1, kWeightFP32>,
                                                           kChunksPerRow, 0);
@@ -717,13 +854,34 @@ cudaError_t launch_tp_cluster(const TpArgs &a, int wk, cudaStream_t s) {
     }
 }
 
-cudaError_t launch_tp_bulk(const TpArgs &a, int wk, cudaStream_t s) {
-    const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(kBulkThreads);
+int64_t tp_bulk_groups(int64_t num_tokens, int64_t resident) {
+    const int64_t n = kBulkTokensPerCta, singles = int64_t{kBulkSingleWaves} * resident;
+    if (resident <= 0 || num_tokens < singles + n * resident) return 0;
+    int64_t groups = (num_tokens - singles) / n;
+    // a partial wave of multi-token CTAs that would end after the one-token CTAs
+    // have run out (it starts one wave of multi-token CTAs late) is dropped
+    const int64_t r = groups % resident;
+    if (r != 0 && n * (resident - r) > singles) groups -= r;
+    return groups;
+}
+
+cudaError_t launch_tp_bulk(const TpArgs &a, int wk, int resident_ctas, cudaStream_t s) {
+    const int64_t groups = tp_bulk_groups(a.num_tokens, resident_ctas);
     const bool p = a.programmatic;
+    const dim3 block(kBulkThreads);
+    if (groups == 0) {
+        const dim3 grid(static_cast<unsigned>(a.num_tokens));
+        switch (wk) {
+            case kWeightBF16: return launch_ex(tp_token_bulk_kernel<kWeightBF16>, grid, block, kBulkSmem, s, 1, p, a);
+            case kWeightPacked: return launch_ex(tp_token_bulk_kernel<kWeightPacked>, grid, block, kBulkSmem, s, 1, p, a);
+            default: return launch_ex(tp_token_bulk_kernel<kWeightFP32>, grid, block, kBulkSmem, s, 1, p, a);
+        }
+    }
+    const dim3 grid(static_cast<unsigned>(a.num_tokens - (kBulkTokensPerCta - 1) * groups));
     switch (wk) {
-        case kWeightBF16: return launch_ex(tp_token_bulk_kernel<kWeightBF16>, grid, block, kBulkSmem, s, 1, p, a);
-        case kWeightPacked: return launch_ex(tp_token_bulk_kernel<kWeightPacked>, grid, block, kBulkSmem, s, 1, p, a);
-        default: return launch_ex(tp_token_bulk_kernel<kWeightFP32>, grid, block, kBulkSmem, s, 1, p, a);
+        case kWeightBF16: return launch_ex(tp_token_bulk_multi_kernel<kWeightBF16>, grid, block, kBulkSmem, s, 1, p, a, groups);
+        case kWeightPacked: return launch_ex(tp_token_bulk_multi_kernel<kWeightPacked>, grid, block, kBulkSmem, s, 1, p, a, groups);
+        default: return launch_ex(tp_token_bulk_multi_kernel<kWeightFP32>, grid, block, kBulkSmem, s, 1, p, a, groups);
     }
 }
 

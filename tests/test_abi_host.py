@@ -243,3 +243,20 @@ def test_binding_rejects_gemm2_narrower_than_hidden(monkeypatch):
                                 torch.ones(4096, dtype=torch.bfloat16),
                                 torch.empty((2, 4096), dtype=torch.bfloat16),
                                 eps=1e-6, gain_center=0.0, weight_before_norm=False)
+
+
+def test_kernel_names_without_a_device(lib):
+    # the launch a call would make, by size and variant; without a device the
+    # wave tests of the automatic choice are skipped
+    name = lambda *a: lib.mf_finalize_kernel_name(*a).decode()
+    assert name(1, 4096, 8, 0) == name(8, 4096, 8, 3) == "tp_cluster_kernel"
+    assert name(16, 4096, 8, 0) == name(9, 4096, 8, 1) == "tp_token_cta_kernel"
+    assert name(5000, 4096, 8, 2) in ("tp_token_bulk_kernel", "tp_token_bulk_multi_kernel")
+    assert name(100, 512, 32, 0) == "tp_warp_bulk_kernel"
+    assert name(100, 1280, 8, 2) == "tp_generic_bulk_kernel"
+    assert name(0, 4096, 8, 0) == name(5, 300, 8, 0) == name(5, 512, 8, 1) == ""
+    beam = lambda *a: lib.mf_beam_kernel_name(*a).decode()
+    assert beam(10, 8, 7168, 0, 0) == beam(10, 8, 7168, 1, 1) == "beam_token_bulk_kernel"
+    assert beam(10, 8, 7168, 1, 0) == "beam_token_cta_kernel"
+    assert beam(10, 8, 512, 0, 0) == "beam_warp_bulk_kernel"
+    assert beam(0, 8, 512, 0, 0) == beam(10, 33, 512, 0, 0) == ""

@@ -127,6 +127,41 @@ def test_ragged_token_counts(cuda_lib, T, variant):
     compare_bf16(run_tp(cuda_lib, case, variant), oracle_tp(case))
 
 
+# Token counts around the multi-token CTAs of the staged hidden-4096 kernel,
+# used from five waves of resident CTAs up (152 SMs x 3 CTAs = 456 on GB300:
+# 2280 tokens is the first multi-token launch; 2600 drops a partial wave of
+# multi-token CTAs, 3284 keeps one).  Rows of stride 4160 with NaN padding
+# columns and padding rows; 5% invalid slots, so a row's mbarrier skips
+# tokens and its phase must still be tracked.
+@pytest.mark.parametrize("T", [2279, 2280, 2281, 2600, 3284, 4567, 9001])
+@pytest.mark.parametrize("wdt", ["fp32", "bf16", "packed"])
+def test_multi_token_ctas(cuda_lib, T, wdt):
+    case = si.tp_case(f"multi{T}{wdt}", T, indexed_rows=T * 8, padding_rows=64, row_stride=4160,
+                      invalid_frac=0.05, weights_dtype=wdt, weight_before_norm=T % 2 == 1,
+                      seed=T, poison_padding=True)
+    assert cuda_lib.select_finalize_variant(T) == "bulk"
+    compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
+
+
+def test_kernel_name_reports_the_multi_token_kernel(cuda_lib):
+    # five waves of the staged kernel's resident CTAs (three per SM) and more
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    first = 5 * 3 * sms
+    assert cuda_lib.finalize_kernel_name(first - 1) == "tp_token_bulk_kernel"
+    assert cuda_lib.finalize_kernel_name(first) == "tp_token_bulk_multi_kernel"
+    assert cuda_lib.finalize_kernel_name(32768) == "tp_token_bulk_multi_kernel"
+    assert cuda_lib.finalize_kernel_name(32768, variant="token_cta") == "tp_token_cta_kernel"
+    assert cuda_lib.beam_kernel_name(8000, 8, 7168, residual=True) == "beam_token_bulk_kernel"
+
+
+def test_multi_token_ctas_half_the_slots_invalid(cuda_lib):
+    # many slots skipped in a row: the per-row phases diverge across tokens
+    T = 3500
+    case = si.tp_case("multi_sparse", T, indexed_rows=T * 8, invalid_frac=0.5,
+                      weights_dtype="fp32", seed=7)
+    compare_bf16(run_tp(cuda_lib, case, "bulk"), oracle_tp(case))
+
+
 def test_fewer_tokens_than_sms(cuda_lib):
     case = small_case(5, seed=5)
     for v in ("bulk", "token_cta", "cluster"):
