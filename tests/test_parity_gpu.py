@@ -319,6 +319,17 @@ def test_beam_shapes(cuda_lib, K, H, variant):
     compare_bf16(run_beam(cuda_lib, case, variant), oracle_beam(case))
 
 
+# Beam launches of many waves with the token in one staged piece, at hidden
+# 2048-7168 with two chunks per thread or one (2304), dead rows poisoned.
+@pytest.mark.parametrize("T,H,K", [(1600, 7168, 8), (6000, 2048, 8), (4000, 4096, 4),
+                                   (3000, 2304, 8)])
+def test_beam_many_waves(cuda_lib, T, H, K):
+    case = si.beam_case(f"bwaves{T}", T + 7, K, H, T, routed_scale=2.5, seed=T + H,
+                        poison_dead_rows=True)
+    assert cuda_lib.beam_kernel_name(T, K, H) == "beam_token_bulk_kernel"
+    compare_bf16(run_beam(cuda_lib, case, "auto"), oracle_beam(case))
+
+
 @pytest.mark.parametrize("variant", BEAM_VARIANTS)
 def test_beam_without_norm_is_bit_exact(cuda_lib, variant):
     case = si.beam_case("beam_nonorm", 300, 8, 7168, 290, routed_scale=2.5, post_weight=False,
@@ -550,6 +561,26 @@ def test_residual_norm_shapes_and_in_place(cuda_lib, K, H):
                             inplace=True)
     rh, rn = oracle.beam_moe_finalize_norm_residual_norm(
         case.expert_outputs, case.weights, res, routed_scale=1.5, post_weight=case.post_weight,
+        post_eps=1e-6, next_weight=case.post_weight[::-1].copy(), next_eps=1e-5,
+        scales=(1.25, -0.75))
+    eh, en = residual_bounds(case, rh, rn, post=True, scales=(1.25, -0.75), next_eps=1e-5,
+                             next_weight=case.post_weight[::-1].copy())
+    compare_bf16(h, rh, extra=eh)
+    compare_bf16(n, rn, extra=en)
+
+
+@pytest.mark.parametrize("inplace", [False, True])
+def test_residual_norm_many_waves(cuda_lib, inplace):
+    # 1600 tokens at 7168 x 8 (five waves and more), in place and not
+    cap, K, H, T = 1603, 8, 7168, 1600
+    case = si.beam_case("resid_waves", cap, K, H, T, routed_scale=2.5, seed=64,
+                        poison_dead_rows=True)
+    assert cuda_lib.beam_kernel_name(T, K, H, residual=True) == "beam_token_bulk_kernel"
+    res = si.normal_bf16((T, H), 1.0, 65, 1)
+    h, n, nw = run_residual(cuda_lib, case, res, post=True, nxt="weighted", scales=(1.25, -0.75),
+                            inplace=inplace)
+    rh, rn = oracle.beam_moe_finalize_norm_residual_norm(
+        case.expert_outputs, case.weights, res, routed_scale=2.5, post_weight=case.post_weight,
         post_eps=1e-6, next_weight=case.post_weight[::-1].copy(), next_eps=1e-5,
         scales=(1.25, -0.75))
     eh, en = residual_bounds(case, rh, rn, post=True, scales=(1.25, -0.75), next_eps=1e-5,
