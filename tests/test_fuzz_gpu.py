@@ -50,6 +50,25 @@ def test_fuzz_finalize(cuda_lib, seed):
         compare_bf16(run_tp(cuda_lib, case, v), ref)
 
 
+@pytest.mark.parametrize("seed", _seeds(8))
+def test_fuzz_finalize_multi_token(cuda_lib, seed):
+    # hidden 4096 / top-k 8 at token counts where the staged kernel takes three
+    # tokens per CTA (from five waves of resident CTAs: 2280 on GB300)
+    rng = np.random.default_rng(5000 + seed)
+    T = int(rng.integers(2280, 6001))
+    case = si.tp_case(f"fuzz_multi{seed}", T, indexed_rows=T * 8 + int(rng.integers(0, 50)),
+                      padding_rows=int(rng.integers(0, 5)),
+                      row_stride=4096 + 8 * int(rng.integers(0, 4)),
+                      sigma=float(rng.choice([0.5, 1.0, 3.0])),
+                      invalid_frac=float(rng.choice([0.0, 0.05, 0.5])),
+                      weights_dtype=str(rng.choice(["fp32", "bf16", "packed"])),
+                      gain_center=float(rng.choice([0.0, 1.0, -0.5])),
+                      eps=float(rng.choice([1e-6, 1e-5, 0.1])),
+                      weight_before_norm=bool(rng.random() < 0.5), seed=seed,
+                      poison_padding=True)
+    compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
+
+
 @pytest.mark.parametrize("seed", _seeds(24))
 def test_fuzz_beam(cuda_lib, seed):
     rng = np.random.default_rng(2000 + seed)

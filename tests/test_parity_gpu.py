@@ -162,6 +162,95 @@ def test_multi_token_ctas_half_the_slots_invalid(cuda_lib):
     compare_bf16(run_tp(cuda_lib, case, "bulk"), oracle_tp(case))
 
 
+def test_multi_token_ctas_with_and_without_programmatic_launch(cuda_lib):
+    case = small_case(3000, seed=44)
+    assert cuda_lib.finalize_kernel_name(3000) == "tp_token_bulk_multi_kernel"
+    try:
+        cuda_lib.set_programmatic_launch(False)
+        off = run_tp(cuda_lib, case, "bulk")
+    finally:
+        cuda_lib.set_programmatic_launch(True)
+    on = run_tp(cuda_lib, case, "bulk")
+    assert np.array_equal(off, on)
+    compare_bf16(on, oracle_tp(case))
+
+
+def test_multi_token_ctas_read_the_previous_calls_output(cuda_lib):
+    # a Beam call writes the 2400 rows that a 3000-token finalize (three tokens
+    # per CTA) gathers right after it on the same stream, with programmatic launch
+    T1, K1, T2 = 2400, 2, 3000
+    beam = si.beam_case("chain_multi", T1, K1, 4096, T1, routed_scale=1.5, post_weight=False,
+                        post_eps=None, seed=45)
+    x, w1 = dev_bf16(beam.expert_outputs), torch.from_numpy(beam.weights).cuda()
+    mid = torch.empty((T1, 4096), dtype=torch.bfloat16, device="cuda")
+    rng = np.random.default_rng(46)
+    idx2 = rng.integers(-1, T1, size=(T2, 8)).astype(np.int32)
+    w2 = rng.random((T2, 8)).astype(np.float32)
+    nw = f32_bits(rng.standard_normal(4096) * 0.1)
+    out = torch.empty((T2, 4096), dtype=torch.bfloat16, device="cuda")
+    idx2_d, w2_d, nw_d = torch.from_numpy(idx2).cuda(), torch.from_numpy(w2).cuda(), dev_bf16(nw)
+    for _ in range(3):
+        mid.fill_(float("nan"))
+        torch.cuda.synchronize()
+        cuda_lib.beam_moe_finalize(x, w1, mid, beam.routed_scale)
+        cuda_lib.moe_finalize_rmsnorm(mid, w2_d, idx2_d, nw_d, out, eps=1e-6, gain_center=1.0,
+                                      weight_before_norm=False)
+        torch.cuda.synchronize()
+        assert not np.isnan(bf16_bits_to_f64(host_bits(out))).any()
+    ref1 = oracle_beam(beam)
+    ref2 = oracle.moe_finalize_rmsnorm(ref1, w2, idx2, nw, eps=1e-6, gain_center=1.0,
+                                       weight_before_norm=False)
+    compare_bf16(host_bits(out), ref2)
+
+
+def test_multi_token_ctas_in_a_graph_and_on_two_streams(cuda_lib):
+    cases = [small_case(2600, seed=47), small_case(2600, seed=48)]
+    c0 = cases[0]
+    g, w, idx, nw = (dev_bf16(c0.gemm2), torch.from_numpy(c0.weights).cuda(),
+                     torch.from_numpy(c0.idx).cuda(), dev_bf16(c0.norm_weight))
+    out = torch.empty((2600, 4096), dtype=torch.bfloat16, device="cuda")
+
+    def call():
+        cuda_lib.moe_finalize_rmsnorm(g, w, idx, nw, out, eps=c0.eps, gain_center=c0.gain_center,
+                                      weight_before_norm=c0.weight_before_norm)
+    call()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st), torch.cuda.graph(graph, stream=st):
+        call()
+    torch.cuda.synchronize()
+    for c in cases:
+        g.copy_(dev_bf16(c.gemm2))
+        w.copy_(torch.from_numpy(c.weights).cuda())
+        idx.copy_(torch.from_numpy(c.idx).cuda())
+        nw.copy_(dev_bf16(c.norm_weight))
+        out.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        compare_bf16(host_bits(out), oracle_tp(c))
+    # two launches in flight at once on two streams, different buffers
+    c1 = cases[1]
+    g1, w1, i1 = dev_bf16(c1.gemm2), torch.from_numpy(c1.weights).cuda(), torch.from_numpy(c1.idx).cuda()
+    nw1 = dev_bf16(c1.norm_weight)
+    out1 = torch.empty_like(out)
+    g.copy_(dev_bf16(c0.gemm2))
+    w.copy_(torch.from_numpy(c0.weights).cuda())
+    idx.copy_(torch.from_numpy(c0.idx).cuda())
+    nw.copy_(dev_bf16(c0.norm_weight))
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        cuda_lib.moe_finalize_rmsnorm(g, w, idx, nw, out, eps=c0.eps, gain_center=c0.gain_center,
+                                      weight_before_norm=c0.weight_before_norm, stream=s1)
+        cuda_lib.moe_finalize_rmsnorm(g1, w1, i1, nw1, out1, eps=c1.eps, gain_center=c1.gain_center,
+                                      weight_before_norm=c1.weight_before_norm, stream=s2)
+    torch.cuda.synchronize()
+    compare_bf16(host_bits(out), oracle_tp(c0))
+    compare_bf16(host_bits(out1), oracle_tp(c1))
+
+
 def test_fewer_tokens_than_sms(cuda_lib):
     case = small_case(5, seed=5)
     for v in ("bulk", "token_cta", "cluster"):
