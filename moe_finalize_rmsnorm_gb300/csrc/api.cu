@@ -178,7 +178,8 @@ mf_status moe_finalize_rmsnorm_variant(const void *gemm2_permuted, int64_t rows,
                                                     : mf::kWeightPacked;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    if (!specialised) return from_launch(mf::launch_tp_generic(a, wk, d->smem_per_sm, s));
+    if (!specialised)
+        return from_launch(mf::launch_tp_generic(a, wk, d->smem_per_sm, d->num_sms, s));
     if (variant == MF_VARIANT_AUTO) variant = pick_tp(num_tokens, d);
     switch (variant) {
         case MF_VARIANT_CLUSTER: return from_launch(mf::launch_tp_cluster(a, wk, s));
@@ -328,7 +329,13 @@ const char *mf_finalize_kernel_name(int64_t num_tokens, int32_t hidden, int32_t 
     if (hidden != mf::kTpHidden || top_k != mf::kTpTopK) {
         if (hidden < 256 || hidden > 8192 || hidden % 256 != 0 || top_k < 1 || top_k > 32) return "";
         if (variant != MF_VARIANT_AUTO && variant != MF_VARIANT_BULK) return "";
-        return hidden <= 1024 ? "tp_warp_bulk_kernel" : "tp_generic_bulk_kernel";
+        if (hidden <= 1024) return "tp_warp_bulk_kernel";
+        const DeviceInfo *d = nullptr;
+        if (device_info(&d) == MF_OK &&
+            mf::tp_generic_groups(num_tokens, hidden, top_k, mf::kWeightFP32, d->smem_per_sm,
+                                  d->num_sms) > 0)
+            return "tp_generic_bulk_multi_kernel";
+        return "tp_generic_bulk_kernel";
     }
     const DeviceInfo *d = nullptr;
     if (device_info(&d) != MF_OK) d = nullptr;

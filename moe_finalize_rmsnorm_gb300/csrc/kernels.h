@@ -80,7 +80,11 @@ cudaError_t launch_tp_bulk(const TpArgs &a, int weight_kind, int resident_ctas, 
 // per CTA throughout).
 int64_t tp_bulk_groups(int64_t num_tokens, int64_t resident_ctas);
 // Any hidden in 256..8192 (multiple of 256) and top-k in 1..32.
-cudaError_t launch_tp_generic(const TpArgs &a, int weight_kind, int smem_per_sm, cudaStream_t s);
+cudaError_t launch_tp_generic(const TpArgs &a, int weight_kind, int smem_per_sm, int num_sms,
+                              cudaStream_t s);
+// Multi-token CTAs of a generic staged launch (0: one token per CTA throughout).
+int64_t tp_generic_groups(int64_t num_tokens, int hidden, int top_k, int weight_kind,
+                          int smem_per_sm, int num_sms);
 
 cudaError_t launch_beam_token_cta(const BeamArgs &a, cudaStream_t s);
 // `residual`: finalize, then the residual-add and next norm of

@@ -654,6 +654,145 @@ __global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks
     }
 }
 
+// The generic staged kernel with several tokens per CTA, for launches of five
+// waves and more whose tokens fit the buffer in one piece (top_k <= the rows
+// per piece) with a barrier per row.  As in tp_token_bulk_multi_kernel, CTA
+// b < groups takes kGenericTokensPerCta consecutive tokens and the CTAs of the
+// last two waves one each; warp 0 loads the next token's route while the
+// current rows land, and once every thread has read them the lane of each
+// valid slot of the next token copies its row into the buffer slot of its rank
+// before the current token's norm and stores.  The compacted weights and the
+// valid count alternate between two buffers.  Each token's arithmetic is that
+// of tp_generic_bulk_kernel: the same bits.
+constexpr int kGenericTokensPerCta = 3;
+constexpr int kGenericSingleWaves = 2;  // waves of one-token CTAs at the end
+
+template <int CPT, int WK>
+__global__ void __launch_bounds__(generic_max_threads<CPT>(), generic_min_blocks<CPT>())
+    tp_generic_bulk_multi_kernel(const TpArgs a, const int rows_per_piece, const int64_t groups) {
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    __shared__ uint64_t bars[32];
+    __shared__ float red[2][32];
+    __shared__ float wc_s[2][32];  // weights of the valid slots, in rank order
+    __shared__ int nvalid_s[2];
+
+    const int NT = blockDim.x;
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.x;
+    const bool grouped = b < groups;
+    int64_t t = grouped ? kGenericTokensPerCta * b : (kGenericTokensPerCta - 1) * groups + b;
+    const int ntok = grouped ? kGenericTokensPerCta : 1;
+    const int H = a.hidden, K = a.top_k;
+    const uint32_t row_bytes = static_cast<uint32_t>(H) * 2;
+    const uint32_t base = smem_u32(rows_smem);
+
+    // warp 0, lane k: slot k of token `tok` -- record its weight by rank and copy
+    // its row into buffer slot `rank` (all of a token's valid rows fit)
+    auto place = [&](int i, bool valid, float w, int buf) {
+        const unsigned mask = __ballot_sync(0xffffffffu, valid);
+        const int rank = __popc(mask & ((1u << tid) - 1u));
+        if (valid) {
+            wc_s[buf][rank] = w;
+            const uint32_t bb = smem_u32(&bars[rank]);
+            mbar_arrive_expect_tx(bb, row_bytes);
+            bulk_copy_g2s_hint(base + rank * row_bytes, a.gemm2 + static_cast<int64_t>(i) * a.ld,
+                               row_bytes, bb, policy_evict_first());
+        }
+        if (tid == 0) nvalid_s[buf] = __popc(mask);
+    };
+    if (tid < rows_per_piece) {
+        mbar_init(smem_u32(&bars[tid]), 1);
+        fence_mbar_init();
+    }
+    pdl_wait();
+    if (tid < 32) {
+        int i = -1;
+        if (tid < K) i = __ldg(a.idx + t * K + tid);
+        const bool valid = tid < K && slot_valid(i, a.rows);
+        const float w = valid ? load_weight<WK>(a.weights, t * K + tid) : 0.f;
+        __syncwarp();
+        place(i, valid, w, 0);
+    }
+    float g[CPT][8];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) load_gain(a, tid + c * NT, g[c]);
+    __syncthreads();
+
+    const bool before = a.before != 0;
+    uint32_t parity = 0;  // bit r: the phase of bars[r] the next wait is for
+    for (int j = 0; j < ntok; ++j, ++t) {
+        const int buf = j & 1;
+        const int nvalid = nvalid_s[buf];
+        int ni = -1;  // warp 0: the next token's route, while this token's rows land
+        bool nvalid_slot = false;
+        float nwt = 0.f;
+        if (j + 1 < ntok && tid < 32) {
+            if (tid < K) ni = __ldg(a.idx + (t + 1) * K + tid);
+            nvalid_slot = tid < K && slot_valid(ni, a.rows);
+            nwt = nvalid_slot ? load_weight<WK>(a.weights, (t + 1) * K + tid) : 0.f;
+        }
+        float acc[CPT][8];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[c][e] = 0.f;
+        bool ok = true;
+        for (int r = 0; r < nvalid; ++r) {
+            const uint32_t bb = smem_u32(&bars[r]);
+            const uint32_t ph = (parity >> r) & 1u;
+            if (!mbar_wait(bb, ph, a.timeout_ns)) {
+                atomicOr(a.status, kStatusWaitTimeout);
+                ok = false;
+                (void)mbar_wait(bb, ph, a.timeout_ns);  // bounded: the copy may land, or not, before exit
+            }
+            const float w = wc_s[buf][r];
+            const uint32_t row = base + r * row_bytes;
+            uint4 q[CPT];
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) q[c] = lds_16(row + (tid + c * NT) * kChunkBytes);
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) {
+                float x[8];
+                unpack8(q[c], x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[c][e] = __fmaf_rn(w, x[e], acc[c][e]);
+            }
+        }
+        parity ^= nvalid >= 32 ? 0xffffffffu : ((1u << nvalid) - 1u);  // rows 0..nvalid-1 moved on
+        bool more = false;
+        if (j + 1 < ntok) {
+            // every thread has read the buffer, and none gave up waiting: the
+            // next token's rows go in flight before this token's epilogue
+            more = !__syncthreads_or(!ok);
+            if (more && tid < 32) {
+                fence_proxy_async_smem();  // the reads above come before the copies
+                place(ni, nvalid_slot, nwt, buf ^ 1);
+            }
+        }
+        const float ss = warp_sum(prenorm<CPT>(acc, g, before));
+        if ((tid & 31) == 0) red[buf][tid >> 5] = ss;
+        __syncthreads();
+        float tot = 0.f;
+        const int nw = NT >> 5;
+        for (int i = 0; i < nw; ++i) tot += red[buf][i];
+        const float r = rsqrtf(__fadd_rn(__fdiv_rn(tot, static_cast<float>(H)), a.eps));
+        if (ok) {
+            uint16_t *out_row = a.out + t * H;
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) {
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float sv = __fmul_rn(acc[c][e], r);
+                    y[e] = before ? sv : __fmul_rn(sv, g[c][e]);
+                }
+                st_cs_16(out_row + static_cast<int64_t>(tid + c * NT) * kChunkElems, pack8_rn(y));
+            }
+        }
+        if (!more) break;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // small hidden (256..1024): one warp per token, four tokens per CTA
 
@@ -815,6 +954,12 @@ cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm) {
     if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightBF16, true>, budget);
     if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightFP32, true>, budget);
     if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<2, kWeightPacked, true>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_multi_kernel<1, kWeightBF16>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_multi_kernel<1, kWeightFP32>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_multi_kernel<1, kWeightPacked>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_multi_kernel<2, kWeightBF16>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_multi_kernel<2, kWeightFP32>, budget);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_multi_kernel<2, kWeightPacked>, budget);
     return e;
 }
 
@@ -923,7 +1068,58 @@ static cudaError_t launch_warp_cpw(const TpArgs &a, int wk, cudaStream_t s) {
     }
 }
 
-cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, cudaStream_t s) {
+template <int CPT>
+static int generic_multi_per_sm(int wk, int threads, size_t bytes) {
+    int n = 0;
+    cudaError_t e;
+    switch (wk) {
+        case kWeightBF16: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tp_generic_bulk_multi_kernel<CPT, kWeightBF16>, threads, bytes); break;
+        case kWeightPacked: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tp_generic_bulk_multi_kernel<CPT, kWeightPacked>, threads, bytes); break;
+        default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tp_generic_bulk_multi_kernel<CPT, kWeightFP32>, threads, bytes); break;
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+int64_t tp_generic_groups(int64_t num_tokens, int hidden, int top_k, int wk, int smem_per_sm,
+                          int num_sms) {
+    if (hidden <= 1024 || num_sms <= 0) return 0;  // the warp-per-token kernel
+    const int rows = generic_rows(smem_per_sm, top_k, hidden);
+    if (top_k > rows) return 0;  // a token's rows in one piece (with a barrier per row)
+    if (num_tokens < int64_t{kGenericTokensPerCta + kGenericSingleWaves} * num_sms) return 0;
+    const int cpt = generic_cpt(hidden);
+    const int threads = hidden / 8 / cpt;
+    const size_t bytes = static_cast<size_t>(rows) * hidden * 2;
+    const int per_sm = cpt == 2 ? generic_multi_per_sm<2>(wk, threads, bytes)
+                                : generic_multi_per_sm<1>(wk, threads, bytes);
+    const int64_t resident = int64_t{per_sm} * num_sms;
+    const int64_t n = kGenericTokensPerCta, singles = int64_t{kGenericSingleWaves} * resident;
+    if (resident <= 0 || num_tokens < singles + n * resident) return 0;
+    int64_t groups = (num_tokens - singles) / n;
+    const int64_t r = groups % resident;  // drop a partial wave that would outlast the rest
+    if (r != 0 && n * (resident - r) > singles) groups -= r;
+    return groups;
+}
+
+template <int CPT>
+static cudaError_t launch_generic_multi(const TpArgs &a, int wk, int rows, int64_t groups,
+                                       cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(a.num_tokens - (kGenericTokensPerCta - 1) * groups));
+    const dim3 block(a.hidden / 8 / CPT);
+    const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;
+    const bool p = a.programmatic;
+    switch (wk) {
+        case kWeightBF16: return launch_ex(tp_generic_bulk_multi_kernel<CPT, kWeightBF16>, grid, block, bytes, s, 1, p, a, rows, groups);
+        case kWeightPacked: return launch_ex(tp_generic_bulk_multi_kernel<CPT, kWeightPacked>, grid, block, bytes, s, 1, p, a, rows, groups);
+        default: return launch_ex(tp_generic_bulk_multi_kernel<CPT, kWeightFP32>, grid, block, bytes, s, 1, p, a, rows, groups);
+    }
+}
+
+cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, int num_sms,
+                              cudaStream_t s) {
     // hidden 256..1024: one warp per token
     switch (a.hidden) {
         case 256: return launch_warp_cpw<1>(a, wk, s);
@@ -933,6 +1129,11 @@ cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, cudaStre
         default: break;
     }
     const int rows = generic_rows(smem_per_sm, a.top_k, a.hidden);
+    const int64_t groups = tp_generic_groups(a.num_tokens, a.hidden, a.top_k, wk, smem_per_sm, num_sms);
+    if (groups > 0) {
+        if (generic_cpt(a.hidden) == 2) return launch_generic_multi<2>(a, wk, rows, groups, s);
+        return launch_generic_multi<1>(a, wk, rows, groups, s);
+    }
     if (generic_cpt(a.hidden) == 2) return launch_generic_cpt<2, true>(a, wk, rows, s);  // hidden >= 2048
     if (a.hidden >= kPerRowMinHidden || a.top_k <= kPerRowMaxTopK)
         return launch_generic_cpt<1, true>(a, wk, rows, s);

@@ -364,6 +364,28 @@ def test_generic_sizes(cuda_lib, H, K, wdt):
         compare_bf16(run_tp(cuda_lib, case, v), oracle_tp(case))
 
 
+# Other sizes at five waves and more with a token in one staged piece run
+# several tokens per CTA (tp_generic_bulk_multi_kernel): hidden 7168 x 8 from
+# 1520 tokens on GB300 (two CTAs per SM), 3072 x 8 and 2304 x 8 (one chunk per
+# thread), 1280 x 10 (small rows, ten per piece); 5% invalid slots.
+@pytest.mark.parametrize("T,H,K", [(1600, 7168, 8), (4000, 3072, 8), (5000, 2304, 8),
+                                   (9000, 1280, 10)])
+@pytest.mark.parametrize("wdt", ["fp32", "bf16", "packed"])
+def test_generic_multi_token_ctas(cuda_lib, T, H, K, wdt):
+    case = si.tp_case(f"gmulti{T}{wdt}", T, hidden=H, top_k=K, indexed_rows=T * K + 5,
+                      padding_rows=3, row_stride=H + 8, invalid_frac=0.05, weights_dtype=wdt,
+                      weight_before_norm=T % 2 == 0, seed=T + H, poison_padding=True)
+    assert cuda_lib.finalize_kernel_name(T, H, K) == "tp_generic_bulk_multi_kernel"
+    compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
+
+
+def test_generic_multi_token_ctas_half_the_slots_invalid(cuda_lib):
+    T, H, K = 2000, 7168, 8
+    case = si.tp_case("gmulti_sparse", T, hidden=H, top_k=K, indexed_rows=T * K,
+                      invalid_frac=0.5, weights_dtype="fp32", seed=9)
+    compare_bf16(run_tp(cuda_lib, case, "bulk"), oracle_tp(case))
+
+
 @pytest.mark.parametrize("variant", TP_VARIANTS)
 def test_packed_routing_words_specialised(cuda_lib, variant):
     case = si.tp_case("packed", 300, indexed_rows=2500, invalid_frac=0.03, weights_dtype="packed",
