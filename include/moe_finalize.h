@@ -260,10 +260,10 @@ mf_variant mf_select_beam_variant(int64_t live_tokens, int32_t top_k, int32_t hi
  * "tp_token_cta_kernel", "tp_token_bulk_kernel", "tp_token_bulk_multi_kernel"
  * (the staged kernel with several tokens per CTA, from five waves of tokens
  * up), "tp_generic_bulk_kernel", "tp_generic_bulk_multi_kernel" (other sizes
- * with several tokens per CTA, on the same rule) or "tp_warp_bulk_kernel".  The
- * empty string
- * when nothing would launch (no tokens, unsupported sizes, a variant that does
- * not apply).  Static string. */
+ * with several tokens per CTA, on the same rule), "tp_warp_bulk_kernel" or
+ * "tp_warp_bulk_multi_kernel" (hidden 256..1024, several tokens per warp).
+ * The empty string when nothing would launch (no tokens, unsupported sizes, a
+ * variant that does not apply).  Static string. */
 const char *mf_finalize_kernel_name(int64_t num_tokens, int32_t hidden, int32_t top_k,
                                     mf_variant variant);
 

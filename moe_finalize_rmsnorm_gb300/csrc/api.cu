@@ -329,13 +329,17 @@ const char *mf_finalize_kernel_name(int64_t num_tokens, int32_t hidden, int32_t 
     if (hidden != mf::kTpHidden || top_k != mf::kTpTopK) {
         if (hidden < 256 || hidden > 8192 || hidden % 256 != 0 || top_k < 1 || top_k > 32) return "";
         if (variant != MF_VARIANT_AUTO && variant != MF_VARIANT_BULK) return "";
-        if (hidden <= 1024) return "tp_warp_bulk_kernel";
         const DeviceInfo *d = nullptr;
-        if (device_info(&d) == MF_OK &&
-            mf::tp_generic_groups(num_tokens, hidden, top_k, mf::kWeightFP32, d->smem_per_sm,
-                                  d->num_sms) > 0)
-            return "tp_generic_bulk_multi_kernel";
-        return "tp_generic_bulk_kernel";
+        if (device_info(&d) != MF_OK) d = nullptr;
+        if (hidden <= 1024)
+            return d != nullptr && mf::tp_warp_groups(num_tokens, hidden, top_k, mf::kWeightFP32,
+                                                      d->num_sms) > 0
+                       ? "tp_warp_bulk_multi_kernel"
+                       : "tp_warp_bulk_kernel";
+        return d != nullptr && mf::tp_generic_groups(num_tokens, hidden, top_k, mf::kWeightFP32,
+                                                     d->smem_per_sm, d->num_sms) > 0
+                   ? "tp_generic_bulk_multi_kernel"
+                   : "tp_generic_bulk_kernel";
     }
     const DeviceInfo *d = nullptr;
     if (device_info(&d) != MF_OK) d = nullptr;

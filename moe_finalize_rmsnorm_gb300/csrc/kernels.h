@@ -82,6 +82,9 @@ int64_t tp_bulk_groups(int64_t num_tokens, int64_t resident_ctas);
 // Any hidden in 256..8192 (multiple of 256) and top-k in 1..32.
 cudaError_t launch_tp_generic(const TpArgs &a, int weight_kind, int smem_per_sm, int num_sms,
                               cudaStream_t s);
+// Multi-token warps of a warp-per-token launch, hidden 256..1024 (0: one token
+// per warp throughout).
+int64_t tp_warp_groups(int64_t num_tokens, int hidden, int top_k, int weight_kind, int num_sms);
 // Multi-token CTAs of a generic staged launch (0: one token per CTA throughout).
 int64_t tp_generic_groups(int64_t num_tokens, int hidden, int top_k, int weight_kind,
                           int smem_per_sm, int num_sms);

@@ -890,6 +890,130 @@ __global__ void __launch_bounds__(32 * warp_tokens_per_cta<CPW>())
     scale_store<CPW, 32>(acc, g, before, r, a.out + t * H, lane);
 }
 
+// The warp-per-token kernel with several tokens per warp, for launches of five
+// waves of resident warps and more whose tokens fit the warp's slice in one
+// piece (top_k <= rows per piece).  Warp u < groups (counted over the grid,
+// two per CTA) takes kWarpMultiTokens consecutive tokens, the warps of the
+// last two waves one each.  A warp loads the next token's route while the
+// current rows land and, once its lanes have read them, copies the next
+// token's rows into its slice before the current token's norm and stores.  The
+// warp's mbarrier moves to its next phase only for tokens with valid rows.
+// Each token's arithmetic is that of tp_warp_bulk_kernel: the same bits.
+constexpr int kWarpMultiTokens = 3;
+constexpr int kWarpSingleWaves = 2;  // waves of one-token warps at the end
+
+template <int CPW, int WK>
+__global__ void __launch_bounds__(32 * warp_tokens_per_cta<CPW>())
+    tp_warp_bulk_multi_kernel(const TpArgs a, const int rows_per_piece, const int64_t groups) {
+    constexpr int kWarpTokensPerCta = warp_tokens_per_cta<CPW>();
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    __shared__ uint64_t bars[kWarpTokensPerCta];
+    constexpr int H = 256 * CPW;
+    constexpr uint32_t row_bytes = H * 2;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t u = static_cast<int64_t>(blockIdx.x) * kWarpTokensPerCta + warp;
+    const bool grouped = u < groups;
+    int64_t t = grouped ? kWarpMultiTokens * u : (kWarpMultiTokens - 1) * groups + u;
+    if (t >= a.num_tokens) return;
+    const int ntok = grouped ? kWarpMultiTokens : 1;
+    const int K = a.top_k;
+    const uint32_t base = smem_u32(rows_smem) + warp * rows_per_piece * row_bytes;
+    const uint32_t bar = smem_u32(&bars[warp]);
+
+    if (lane == 0) {
+        mbar_init(bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    // this warp's copies of token `tok`'s valid rows, each by the lane of its
+    // slot, into the slice position of its rank
+    auto issue = [&](int i, bool valid, unsigned mask) {
+        const int nv = __popc(mask);
+        if (nv == 0) return;
+        if (lane == 0) mbar_arrive_expect_tx(bar, nv * row_bytes);
+        __syncwarp();
+        if (valid)
+            bulk_copy_g2s_hint(base + __popc(mask & ((1u << lane) - 1u)) * row_bytes,
+                               a.gemm2 + static_cast<int64_t>(i) * a.ld, row_bytes, bar,
+                               policy_evict_first());
+    };
+
+    pdl_wait();
+    int my_idx = -1;
+    if (lane < K) my_idx = __ldg(a.idx + t * K + lane);
+    bool valid = lane < K && slot_valid(my_idx, a.rows);
+    float my_w = valid ? load_weight<WK>(a.weights, t * K + lane) : 0.f;
+    unsigned mask = __ballot_sync(0xffffffffu, valid);
+    issue(my_idx, valid, mask);
+    float g[CPW][8];
+#pragma unroll
+    for (int c = 0; c < CPW; ++c) load_gain(a, lane + c * 32, g[c]);
+
+    const bool before = a.before != 0;
+    uint32_t phase = 0;
+    for (int j = 0; j < ntok; ++j, ++t) {
+        int nidx = -1;  // the next token's route, while this token's rows land
+        bool nvalid = false;
+        float nw = 0.f;
+        if (j + 1 < ntok) {
+            if (lane < K) nidx = __ldg(a.idx + (t + 1) * K + lane);
+            nvalid = lane < K && slot_valid(nidx, a.rows);
+            nw = nvalid ? load_weight<WK>(a.weights, (t + 1) * K + lane) : 0.f;
+        }
+        float acc[CPW][8];
+#pragma unroll
+        for (int c = 0; c < CPW; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[c][e] = 0.f;
+        bool ok = true;
+        if (mask != 0u) {
+            if (!mbar_wait(bar, phase, a.timeout_ns)) {
+                atomicOr(a.status, kStatusWaitTimeout);
+                ok = false;
+                (void)mbar_wait(bar, phase, a.timeout_ns);  // bounded: the copies may land, or not, before exit
+            }
+            phase ^= 1u;
+            unsigned rest = mask;
+            const int n = __popc(mask);
+            for (int r = 0; r < n; ++r) {
+                const int k = __ffs(rest) - 1;
+                rest &= rest - 1;
+                const float w = __shfl_sync(0xffffffffu, my_w, k);
+                const uint32_t row = base + r * row_bytes;
+                uint4 q[CPW];
+#pragma unroll
+                for (int c = 0; c < CPW; ++c) q[c] = lds_16(row + (lane + c * 32) * kChunkBytes);
+#pragma unroll
+                for (int c = 0; c < CPW; ++c) {
+                    float x[8];
+                    unpack8(q[c], x);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[c][e] = __fmaf_rn(w, x[e], acc[c][e]);
+                }
+            }
+        }
+        bool more = false;
+        if (j + 1 < ntok) {
+            // every lane has read the slice, and none gave up waiting: the next
+            // token's rows go in flight before this token's epilogue
+            more = __all_sync(0xffffffffu, ok);
+            if (more) {
+                fence_proxy_async_smem();  // the reads above come before the copies
+                const unsigned nmask = __ballot_sync(0xffffffffu, nvalid);
+                issue(nidx, nvalid, nmask);
+                my_idx = nidx;
+                valid = nvalid;
+                mask = nmask;
+            }
+        }
+        const float tot = warp_sum(prenorm<CPW>(acc, g, before));
+        const float r = rsqrtf(__fadd_rn(__fdiv_rn(tot, static_cast<float>(H)), a.eps));
+        if (ok) scale_store<CPW, 32>(acc, g, before, r, a.out + t * H, lane);
+        if (!more) break;
+        my_w = nw;
+    }
+}
+
 // 2 chunks per thread when that leaves at least 128 threads (hidden 2048 and
 // up, an even number of 256-column groups), else 1.  At hidden 2048-3584 two
 // chunks per thread measured 1-7 % faster than one (fewer threads wait on each
@@ -945,6 +1069,18 @@ cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm) {
     if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<4, kWeightBF16>, warp_smem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<4, kWeightFP32>, warp_smem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<4, kWeightPacked>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<1, kWeightBF16>, warp_smem1);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<1, kWeightFP32>, warp_smem1);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<1, kWeightPacked>, warp_smem1);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<2, kWeightBF16>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<2, kWeightFP32>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<2, kWeightPacked>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<3, kWeightBF16>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<3, kWeightFP32>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<3, kWeightPacked>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<4, kWeightBF16>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<4, kWeightFP32>, warp_smem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_multi_kernel<4, kWeightPacked>, warp_smem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightBF16, false>, budget);
     if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightFP32, false>, budget);
     if (e == cudaSuccess) e = set_dyn_smem(tp_generic_bulk_kernel<1, kWeightPacked, false>, budget);
@@ -1049,18 +1185,67 @@ static cudaError_t launch_generic_cpt(const TpArgs &a, int wk, int rows, cudaStr
 constexpr int kPerRowMinHidden = 2048;
 constexpr int kPerRowMaxTopK = 16;
 
-template <int CPW>
-static cudaError_t launch_warp_cpw(const TpArgs &a, int wk, cudaStream_t s) {
-    constexpr int kWarpTokensPerCta = warp_tokens_per_cta<CPW>();
-    // at least 8 rows per piece and up to 8 KB of them (hidden 256 x 32: 16 rows,
-    // 0.95 of the copy peak against 0.82 with 32; hidden 1024: 8 rows, 16 KB)
-    int rows = 8192 / (a.hidden * 2);
+// Rows per piece of the warp-per-token kernels: at least 8 and up to 8 KB of
+// them (hidden 256 x 32: 16 rows, 0.95 of the copy peak against 0.82 with 32;
+// hidden 1024: 8 rows, 16 KB)
+static int warp_rows(int hidden, int top_k) {
+    int rows = 8192 / (hidden * 2);
     if (rows < 8) rows = 8;
-    if (rows > a.top_k) rows = a.top_k;
-    const dim3 grid(static_cast<unsigned>((a.num_tokens + kWarpTokensPerCta - 1) / kWarpTokensPerCta));
+    return rows > top_k ? top_k : rows;
+}
+
+template <int CPW>
+static int warp_multi_per_sm(int wk, size_t bytes) {
+    constexpr int threads = 32 * warp_tokens_per_cta<CPW>();
+    int n = 0;
+    cudaError_t e;
+    switch (wk) {
+        case kWeightBF16: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tp_warp_bulk_multi_kernel<CPW, kWeightBF16>, threads, bytes); break;
+        case kWeightPacked: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tp_warp_bulk_multi_kernel<CPW, kWeightPacked>, threads, bytes); break;
+        default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, tp_warp_bulk_multi_kernel<CPW, kWeightFP32>, threads, bytes); break;
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+// Multi-token warps of a warp-per-token launch (0: one token per warp).
+template <int CPW>
+static int64_t warp_groups(int64_t num_tokens, int top_k, int wk, int num_sms) {
+    constexpr int H = 256 * CPW;
+    const int rows = warp_rows(H, top_k);
+    if (top_k > rows || num_sms <= 0) return 0;  // a token's rows in one piece
+    const size_t bytes = static_cast<size_t>(rows) * H * 2 * warp_tokens_per_cta<CPW>();
+    const int64_t resident =
+        int64_t{warp_multi_per_sm<CPW>(wk, bytes)} * warp_tokens_per_cta<CPW>() * num_sms;
+    const int64_t n = kWarpMultiTokens, singles = int64_t{kWarpSingleWaves} * resident;
+    if (resident <= 0 || num_tokens < singles + n * resident) return 0;
+    int64_t groups = (num_tokens - singles) / n;
+    const int64_t r = groups % resident;  // drop a partial wave that would outlast the rest
+    if (r != 0 && n * (resident - r) > singles) groups -= r;
+    return groups;
+}
+
+template <int CPW>
+static cudaError_t launch_warp_cpw(const TpArgs &a, int wk, int num_sms, cudaStream_t s) {
+    constexpr int kWarpTokensPerCta = warp_tokens_per_cta<CPW>();
+    const int rows = warp_rows(a.hidden, a.top_k);
     const dim3 block(32 * kWarpTokensPerCta);
     const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2 * kWarpTokensPerCta;
     const bool p = a.programmatic;
+    const int64_t groups = warp_groups<CPW>(a.num_tokens, a.top_k, wk, num_sms);
+    if (groups > 0) {
+        const int64_t units = a.num_tokens - (kWarpMultiTokens - 1) * groups;
+        const dim3 mgrid(static_cast<unsigned>((units + kWarpTokensPerCta - 1) / kWarpTokensPerCta));
+        switch (wk) {
+            case kWeightBF16: return launch_ex(tp_warp_bulk_multi_kernel<CPW, kWeightBF16>, mgrid, block, bytes, s, 1, p, a, rows, groups);
+            case kWeightPacked: return launch_ex(tp_warp_bulk_multi_kernel<CPW, kWeightPacked>, mgrid, block, bytes, s, 1, p, a, rows, groups);
+            default: return launch_ex(tp_warp_bulk_multi_kernel<CPW, kWeightFP32>, mgrid, block, bytes, s, 1, p, a, rows, groups);
+        }
+    }
+    const dim3 grid(static_cast<unsigned>((a.num_tokens + kWarpTokensPerCta - 1) / kWarpTokensPerCta));
     switch (wk) {
         case kWeightBF16: return launch_ex(tp_warp_bulk_kernel<CPW, kWeightBF16>, grid, block, bytes, s, 1, p, a, rows);
         case kWeightPacked: return launch_ex(tp_warp_bulk_kernel<CPW, kWeightPacked>, grid, block, bytes, s, 1, p, a, rows);
@@ -1082,6 +1267,16 @@ static int generic_multi_per_sm(int wk, int threads, size_t bytes) {
         return 0;
     }
     return n;
+}
+
+int64_t tp_warp_groups(int64_t num_tokens, int hidden, int top_k, int wk, int num_sms) {
+    switch (hidden) {
+        case 256: return warp_groups<1>(num_tokens, top_k, wk, num_sms);
+        case 512: return warp_groups<2>(num_tokens, top_k, wk, num_sms);
+        case 768: return warp_groups<3>(num_tokens, top_k, wk, num_sms);
+        case 1024: return warp_groups<4>(num_tokens, top_k, wk, num_sms);
+        default: return 0;
+    }
 }
 
 int64_t tp_generic_groups(int64_t num_tokens, int hidden, int top_k, int wk, int smem_per_sm,
@@ -1122,10 +1317,10 @@ cudaError_t launch_tp_generic(const TpArgs &a, int wk, int smem_per_sm, int num_
                               cudaStream_t s) {
     // hidden 256..1024: one warp per token
     switch (a.hidden) {
-        case 256: return launch_warp_cpw<1>(a, wk, s);
-        case 512: return launch_warp_cpw<2>(a, wk, s);
-        case 768: return launch_warp_cpw<3>(a, wk, s);
-        case 1024: return launch_warp_cpw<4>(a, wk, s);
+        case 256: return launch_warp_cpw<1>(a, wk, num_sms, s);
+        case 512: return launch_warp_cpw<2>(a, wk, num_sms, s);
+        case 768: return launch_warp_cpw<3>(a, wk, num_sms, s);
+        case 1024: return launch_warp_cpw<4>(a, wk, num_sms, s);
         default: break;
     }
     const int rows = generic_rows(smem_per_sm, a.top_k, a.hidden);

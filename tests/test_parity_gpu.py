@@ -379,6 +379,30 @@ def test_generic_multi_token_ctas(cuda_lib, T, H, K, wdt):
     compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
 
 
+# Hidden 256..1024 at five waves of resident warps and more, a token in one
+# slice piece (top_k <= 8, or 16 at hidden 256): three tokens per warp
+# (tp_warp_bulk_multi_kernel); the last CTA's second warp may have no token.
+@pytest.mark.parametrize("T,H,K", [(30001, 256, 8), (30000, 256, 16), (25001, 512, 8),
+                                   (15000, 768, 8), (13000, 1024, 6)])
+@pytest.mark.parametrize("wdt", ["fp32", "bf16", "packed"])
+def test_warp_multi_token(cuda_lib, T, H, K, wdt):
+    case = si.tp_case(f"wmulti{T}{H}{wdt}", T, hidden=H, top_k=K, indexed_rows=T * K + 5,
+                      padding_rows=3, row_stride=H + 8, invalid_frac=0.05, weights_dtype=wdt,
+                      weight_before_norm=T % 2 == 1, seed=T + H, poison_padding=True)
+    assert cuda_lib.finalize_kernel_name(T, H, K) == "tp_warp_bulk_multi_kernel"
+    compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
+
+
+def test_warp_multi_token_sparse_and_empty_tokens(cuda_lib):
+    # 60% invalid slots: some tokens have no valid row at all (the warp's
+    # barrier then skips a phase) -- their output is exactly zero
+    T, H, K = 30000, 512, 4
+    case = si.tp_case("wmulti_sparse", T, hidden=H, top_k=K, indexed_rows=T * K,
+                      invalid_frac=0.6, weights_dtype="fp32", seed=10)
+    assert (np.all((case.idx < 0) | (case.idx >= case.gemm2.shape[0]), axis=1)).sum() > 100
+    compare_bf16(run_tp(cuda_lib, case, "bulk"), oracle_tp(case))
+
+
 def test_generic_multi_token_ctas_half_the_slots_invalid(cuda_lib):
     T, H, K = 2000, 7168, 8
     case = si.tp_case("gmulti_sparse", T, hidden=H, top_k=K, indexed_rows=T * K,
