@@ -69,6 +69,23 @@ def test_fuzz_finalize_multi_token(cuda_lib, seed):
     compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
 
 
+@pytest.mark.parametrize("seed", _seeds(8))
+def test_fuzz_finalize_many_tokens_other_sizes(cuda_lib, seed):
+    # other sizes at token counts where the generic and warp-per-token kernels
+    # take several tokens per CTA or warp (when a token fits one piece)
+    rng = np.random.default_rng(6000 + seed)
+    H = int(rng.choice([256, 512, 768, 1024, 1280, 2048, 2304, 3072, 7168]))
+    K = int(rng.integers(1, 17 if H == 256 else 9))
+    T = int(rng.integers(22000, 36000)) if H <= 1024 else int(rng.integers(3100, 9000))
+    case = si.tp_case(f"fuzz_many{seed}", T, hidden=H, top_k=K, indexed_rows=T * K + 7,
+                      padding_rows=int(rng.integers(0, 5)), row_stride=H + 8 * int(rng.integers(0, 4)),
+                      invalid_frac=float(rng.choice([0.0, 0.05, 0.5])),
+                      weights_dtype=str(rng.choice(["fp32", "bf16", "packed"])),
+                      gain_center=float(rng.choice([0.0, 1.0])), eps=float(rng.choice([1e-6, 0.1])),
+                      weight_before_norm=bool(rng.random() < 0.5), seed=seed, poison_padding=True)
+    compare_bf16(run_tp(cuda_lib, case, "auto"), oracle_tp(case))
+
+
 @pytest.mark.parametrize("seed", _seeds(24))
 def test_fuzz_beam(cuda_lib, seed):
     rng = np.random.default_rng(2000 + seed)
