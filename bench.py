@@ -50,6 +50,9 @@ PROFILES = os.path.join(ROOT, "profiles")
 
 # More than twice the GB300's 129 MB L2: the scratch write of --cold.
 L2_FLUSH_BYTES = 288 * 1024 * 1024
+# GB300's L2; a launch's inputs count as cold when the launches since their
+# last use have moved at least four times this much.
+L2_BYTES = 129 * 10 ** 6
 
 
 def rank_seed(base_seed: int, rank: int) -> int:
@@ -754,11 +757,6 @@ def run_ours(args) -> None:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
-
-
-# GB300's L2; a launch's inputs count as cold when the launches since their
-# last use have moved at least four times this much.
-L2_BYTES = 129 * 10 ** 6
 
 
 def input_copies(bytes_per_launch: int) -> int:
