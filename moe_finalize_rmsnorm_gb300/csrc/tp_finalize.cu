@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(kChunksPerRow / C) tp_cluster_kernel(const TpA
     const int chunk = static_cast<int>(rank) * NT + tid;
 
     pdl_wait();
+    pdl_trigger();  // the next call's CTAs may be scheduled now (they still wait for this grid)
     int idx[8];
     float w[8];
     load_route<WK>(a, t, idx, w);
@@ -251,7 +252,6 @@ __global__ void __launch_bounds__(kChunksPerRow / C) tp_cluster_kernel(const TpA
     const float r = rsqrtf(__fmaf_rn(tot, 1.0f / kTpHidden, a.eps));
 
     scale_store<1, 1>(acc, g, before, r, a.out + t * kTpHidden, chunk);
-    pdl_trigger();
     // no CTA leaves while another may still read its `part`; every value read
     // from a peer has been used above, and no peer reads the stores, so the
     // arrive is relaxed (4-6 % less per decode call than release / acquire)
