@@ -37,18 +37,24 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_finalize_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
+# A prebuilt oracle library to load instead (the mutation tests point this at a
+# copy of the oracle with one planted mistake, to check that the pins catch it).
+_OVERRIDE = os.environ.get("MF_ORACLE_SO")
+if _OVERRIDE:
+    _LIB = _OVERRIDE
 _lock = threading.Lock()
 _lib = None
+
+GCC_FLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
 
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (no CUDA, no shared code with the GPU path)."""
+    if _OVERRIDE:
+        return _LIB
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.run(
-            ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-             "-shared", _SRC, "-o", tmp, "-lm"],
-            check=True)
+        subprocess.run(["gcc", *GCC_FLAGS, _SRC, "-o", tmp, "-lm"], check=True)
         os.replace(tmp, _LIB)
     return _LIB
 

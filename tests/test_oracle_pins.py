@@ -444,6 +444,28 @@ def test_reduction_is_fp32_in_slot_order():
     assert vals(out[0]) == [0.0, 1.4140625]
 
 
+def test_reduction_fuses_each_slot_into_one_rounding():
+    # each slot is one fused multiply-add (a single rounding of w * x + acc), the
+    # reading the kernels reproduce bit for bit.  w = 1 + 2^-17 (FP32) on the
+    # BF16 rows x0 = -(1 + 2^-7) and x1 = 1 + 2^-7 (every column):
+    #   slot 0: w * x0 = -(1 + 2^-7 + 2^-17 + 2^-24), rounded (a tie, to even)
+    #           to -(1 + 2^-7 + 2^-17) = acc
+    #   slot 1: fused, w * x1 + acc = 2^-24 exactly; unfused, the product rounds
+    #           to 1 + 2^-7 + 2^-17 first and the sum is 0.
+    # With gain 1 and eps 2^-100, acc = 2^-24 in every column gives y = 1.0;
+    # an unfused reduction gives acc = 0 and y = 0.
+    x = np.array([[-(1 + 2.0 ** -7)] * 4, [1 + 2.0 ** -7] * 4], dtype=np.float32)
+    w = np.full((1, 2), 1 + 2.0 ** -17, dtype=np.float32)
+    idx = np.array([[0, 1]], dtype=np.int32)
+    for before in (False, True):
+        out = oracle.moe_finalize_rmsnorm(bits(x), w, idx, bits([1, 1, 1, 1]), eps=2.0 ** -100,
+                                          gain_center=0.0, weight_before_norm=before)
+        assert vals(out[0]) == [1.0] * 4
+    # the same in Beam's reduction: BF16(2^-24) times scale 1 is 2^-24 exactly
+    beam = oracle.beam_moe_finalize(bits(x)[None, :, :1].copy(), w, 1, routed_scale=1.0)
+    assert vals(beam[0]) == [2.0 ** -24]
+
+
 # --------------------------------------------------------------------------
 # beam_moe_finalize
 
