@@ -59,6 +59,20 @@ MUTATIONS = [
     ("FP32 reduction replaced by a plain multiply-add",
      "acc[h] = fmaf(w, bf16_bits_to_float(x[h]), acc[h]);",
      "acc[h] = acc[h] + w * bf16_bits_to_float(x[h]);", 1),
+    ("gain center added in float64", "float g = bf16_bits_to_float(norm_weight[h]) + gain_center;",
+     "double g = (double)bf16_bits_to_float(norm_weight[h]) + (double)gain_center;", 2),
+    ("Beam scale product in float64",
+     "float scaled = bf16_bits_to_float(rounded) * routed_scale; /* FP32 product */",
+     "double scaled = (double)bf16_bits_to_float(rounded) * (double)routed_scale;", 1),
+    ("residual sum in float64", "float sum = fmaf(scale_residual, r, scale_x * x);",
+     "double sum = (double)scale_residual * r + (double)scale_x * x;", 1),
+    ("routed_scale applied before the first round",
+     "uint16_t rounded = oracle_bf16_from_double((double)acc[h]);",
+     "uint16_t rounded = oracle_bf16_from_double((double)(acc[h] * routed_scale));\n"
+     "            routed_scale = 1.0f;", 1),
+    ("unweighted post norm skipped", "if (!has_post_norm) {",
+     "if (!has_post_norm || !post_weight) {", 1),
+    ("eps divided by hidden", "sum_sq / (double)hidden + eps)", "sum_sq / (double)hidden + eps / hidden)", 1),
 ]
 
 

@@ -466,6 +466,19 @@ def test_reduction_fuses_each_slot_into_one_rounding():
     assert vals(beam[0]) == [2.0 ** -24]
 
 
+def test_gain_center_is_added_in_fp32():
+    # the API page adds gain_center to norm_weight in FP32: with norm_weight 2^-30
+    # and gain_center 1 + 2^-8, the FP32 sum drops 2^-30 (under half an FP32 ulp)
+    # and g = 1 + 2^-8 exactly.  A constant row of ones with weight 1 and eps 0
+    # gives acc / rms = 1, so y = g = 1 + 2^-8: a BF16 tie, to even -> 1.0.  A
+    # float64 add keeps 1 + 2^-8 + 2^-30, which rounds up to 1 + 2^-7.
+    out = oracle.moe_finalize_rmsnorm(bits([[1, 1, 1, 1]]), np.ones((1, 1), dtype=np.float32),
+                                      np.zeros((1, 1), dtype=np.int32),
+                                      bits([2.0 ** -30] * 4), eps=0.0,
+                                      gain_center=1 + 2.0 ** -8, weight_before_norm=False)
+    assert vals(out[0]) == [1.0] * 4
+
+
 # --------------------------------------------------------------------------
 # beam_moe_finalize
 
@@ -476,6 +489,19 @@ def test_beam_identity():
     w = np.ones((5, 1), dtype=np.float32)
     out = oracle.beam_moe_finalize(x, w, 5)
     assert np.array_equal(out, x[:, 0, :])
+
+
+def test_beam_scale_is_an_fp32_product():
+    # the scale multiplies the BF16 sum as PyTorch's BF16 tensor times a scalar:
+    # one FP32 product, then BF16.  r = 1 + 2^-7 and the FP32 scale
+    # s = 16712189 * 2^-24: r * s = 1 + 2^-8 + 5.8e-8 exactly, which FP32 rounds
+    # to 1 + 2^-8 (the excess is under half an FP32 ulp); that is a BF16 tie,
+    # to even -> 1.0.  A float64 product keeps the excess and rounds to 1 + 2^-7.
+    x = bits([[[1 + 2.0 ** -7] * 4]])
+    s = 16712189 * 2.0 ** -24
+    assert float(np.float32(s)) == s
+    out = oracle.beam_moe_finalize(x, np.ones((1, 1), dtype=np.float32), 1, routed_scale=s)
+    assert vals(out[0]) == [1.0] * 4
 
 
 def test_beam_rounds_sum_before_scale():
@@ -628,6 +654,17 @@ def test_residual_scales_hand_example():
     r = bits([[1.0, 2.0, 4.0, -8.0]])
     hid, _ = oracle.beam_moe_finalize_norm_residual_norm(x, w, r, scales=(2.0, 0.5))
     assert vals(hid[0]) == [3.5, 3.0, -2.0, 2.0]
+
+
+def test_residual_sum_is_one_fp32_rounding():
+    # reading: hidden = BF16(fma(s1, r, s0 * x)) in FP32.  x = 1, r = 2^-8 and
+    # scales (1, 1 + 2^-23): s1 * r + x = 1 + 2^-8 + 2^-31 exactly, which FP32
+    # rounds to 1 + 2^-8 (2^-31 is under half an FP32 ulp); that is a BF16 tie,
+    # to even -> 1.0.  A float64 sum rounds to 1 + 2^-7.
+    x, w = _identity_beam([[1.0] * 4])
+    r = bits([[2.0 ** -8] * 4])
+    hid, _ = oracle.beam_moe_finalize_norm_residual_norm(x, w, r, scales=(1.0, 1 + 2.0 ** -23))
+    assert vals(hid[0]) == [1.0] * 4
 
 
 def test_residual_next_norm_closed_form():
