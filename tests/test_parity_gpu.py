@@ -251,6 +251,58 @@ def test_multi_token_ctas_in_a_graph_and_on_two_streams(cuda_lib):
     compare_bf16(host_bits(out1), oracle_tp(c1))
 
 
+def _tie_case(rows, w, nw, *, eps, gc, before, T=3):
+    # T tokens, each gathering the same rows in its first slots; the other of its
+    # 8 slots are invalid (-1), so every hidden-4096 kernel applies
+    n = rows.shape[0]
+    idx = np.full((T, 8), -1, dtype=np.int32)
+    idx[:, :n] = np.arange(n, dtype=np.int32)
+    wt = np.zeros((T, 8), dtype=np.float32)
+    wt[:, :n] = w
+    return si.TpCase("tie", f32_bits(rows), wt, idx, f32_bits(nw), 4096, eps, gc, before)
+
+
+@pytest.mark.parametrize("variant", TP_VARIANTS)
+def test_fp32_rounding_ties_match_the_oracle(cuda_lib, variant):
+    # inputs on which FP32 and float64 arithmetic round to different BF16 values
+    # (derivations in the oracle pins): one rounding per slot of the reduction,
+    # and the FP32 add of the gain center.  Every kernel must give the oracle's
+    # bits exactly: 1.0 in every element.
+    one_plus = np.float32(1 + 2.0 ** -7)
+    fma_rows = np.stack([np.full(4096, -one_plus), np.full(4096, one_plus)]).astype(np.float32)
+    fma_w = np.full(2, 1 + 2.0 ** -17, dtype=np.float32)
+    for before in (False, True):
+        case = _tie_case(fma_rows, fma_w, np.ones(4096), eps=2.0 ** -100, gc=0.0, before=before)
+        got, ref = run_tp(cuda_lib, case, variant), oracle_tp(case)
+        assert np.all(ref == 0x3F80) and np.array_equal(got, ref)
+    case = _tie_case(np.ones((1, 4096), dtype=np.float32), np.ones(1, dtype=np.float32),
+                     np.full(4096, 2.0 ** -30), eps=0.0, gc=1 + 2.0 ** -8, before=False)
+    got, ref = run_tp(cuda_lib, case, variant), oracle_tp(case)
+    assert np.all(ref == 0x3F80) and np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("variant", BEAM_VARIANTS)
+def test_beam_fp32_scale_tie_matches_the_oracle(cuda_lib, variant):
+    # the FP32 product of the BF16 sum and the scale lands exactly on a BF16 tie
+    # (1 + 2^-8 -> 1.0); a float64 product would give 1 + 2^-7
+    x = f32_bits(np.full((4, 1, 256), 1 + 2.0 ** -7, dtype=np.float32))
+    case = si.BeamCase("tie", x, np.ones((4, 1), dtype=np.float32), 4,
+                       16712189 * 2.0 ** -24, None, None, meta={})
+    got, ref = run_beam(cuda_lib, case, variant), oracle_beam(case)
+    assert np.all(ref == 0x3F80) and np.array_equal(got, ref)
+
+
+def test_residual_fp32_sum_tie_matches_the_oracle(cuda_lib):
+    # hidden = BF16(fma(1 + 2^-23, 2^-8, 1)) = BF16(1 + 2^-8) = 1.0 in FP32
+    case = si.BeamCase("tie", f32_bits(np.ones((4, 1, 256), dtype=np.float32)),
+                       np.ones((4, 1), dtype=np.float32), 4, 1.0, None, None, meta={})
+    res = f32_bits(np.full((4, 256), 2.0 ** -8, dtype=np.float32))
+    h, _, _ = run_residual(cuda_lib, case, res, post=False, nxt=None, scales=(1.0, 1 + 2.0 ** -23))
+    rh, _ = oracle.beam_moe_finalize_norm_residual_norm(case.expert_outputs, case.weights, res,
+                                                        scales=(1.0, 1 + 2.0 ** -23))
+    assert np.all(rh == 0x3F80) and np.array_equal(h, rh)
+
+
 def test_fewer_tokens_than_sms(cuda_lib):
     case = small_case(5, seed=5)
     for v in ("bulk", "token_cta", "cluster"):
