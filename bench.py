@@ -750,6 +750,9 @@ def run_ours(args) -> None:
                                 "host_gbs": n * passes / secs * bytes_per_token(kind, case)
                                 / 1e9,
                                 "cpu": host_cpu()}
+    if (rank == 0 and world == 1 and kind == "tp" and case.hidden == 4096 and case.top_k == 8
+            and case.num_tokens >= 1024 and not (args.cold or args.graph)):
+        line["data_movement"] = run_data_movement(torch, mf, job, sets, device)
     if rank == 0 and world == 1 and args.workload == "roofline" and not (
             args.cold or args.graph or args.no_other_configs):
         line["other_configs"] = run_other_configs(torch, mf, device, nvml)
@@ -757,6 +760,51 @@ def run_ours(args) -> None:
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+
+
+def run_data_movement(torch, mf, job: Job, sets, device, rounds: int = 5,
+                      launches: int = 100) -> dict:
+    """The finalize against its own bytes moved with no arithmetic
+    (mf.finalize_data_movement: route, valid rows and output row, one staged CTA
+    per token) on the same buffers.  Blocks of back-to-back launches between one
+    event pair each, the two kernels alternating block by block (launch i reads
+    input copy i mod len(sets), as in the timed region); medians over the rounds."""
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def finalize(i):
+        job.launch(i, tensors=sets[i % len(sets)])
+
+    def data_movement(i):
+        g, w, idx, _nw, out = sets[i % len(sets)]
+        mf.finalize_data_movement(g, w, idx, out)
+
+    def block(fn) -> float:
+        e0.record(stream)
+        for i in range(launches):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) * 1e3 / launches
+
+    for fn in (finalize, data_movement):  # untimed
+        fn(0)
+    torch.cuda.synchronize(device)
+    fin, dm = [], []
+    for _ in range(rounds):
+        fin.append(block(finalize))
+        dm.append(block(data_movement))
+    if mf.device_status(clear=True) != 0:
+        raise SystemExit("device wait timeout in the data-movement comparison")
+    fin_us, dm_us = float(np.median(fin)), float(np.median(dm))
+    return {"kernel": "tp_data_movement_kernel", "finalize_kernel": job.kernel,
+            "rounds": rounds, "launches_per_block": launches,
+            "finalize_us": fin_us, "data_movement_us": dm_us,
+            "data_movement_gbs": job.bytes_per_launch / (dm_us * 1e-6) / 1e9,
+            "finalize_speed_vs_data_movement": dm_us / fin_us,
+            "what": "the finalize's algorithmic bytes moved by a staged kernel with no "
+                    "arithmetic, timed in alternating blocks with the finalize on the same "
+                    "buffers"}
 
 
 def input_copies(bytes_per_launch: int) -> int:

@@ -289,6 +289,24 @@ mf_status mf_device_status(int clear);
  * usable.  Read the result with mf_device_status(). */
 mf_status mf_selftest_wait_timeout(uint64_t timeout_ns, mf_stream_t stream);
 
+/* Measurement aid, not part of the operation: the memory traffic of
+ * moe_finalize_rmsnorm at hidden 4096 and top_k 8, without its arithmetic.
+ * The arguments mean what they mean there (gemm2_permuted BF16 [rows,
+ * row_stride]; expert_weights and expanded_idx_to_permuted_idx [num_tokens,
+ * 8]; output BF16 [num_tokens, 4096], device pointers, 16-byte aligned).  One
+ * CTA per token reads the token's route, copies each valid row into shared
+ * memory, reads it back and stores one 4096-element output row, so the call
+ * moves the same bytes as the finalize; what it stores is a bit pattern of no
+ * meaning (the XOR of the words read).  Timing it beside the finalize on the
+ * same buffers shows what the reduction, the norm and the finalize's kernel
+ * scheduling add to the traffic itself.  Statuses and the bounded waits as
+ * for moe_finalize_rmsnorm (MF_ERR_SHAPE for a row stride under 4096 or not a
+ * multiple of 8, or more than 2^31 - 1 tokens). */
+mf_status mf_finalize_data_movement(const void *gemm2_permuted, int64_t rows, int64_t row_stride,
+                                    const void *expert_weights, mf_dtype weights_dtype,
+                                    const int32_t *expanded_idx_to_permuted_idx, void *output,
+                                    int64_t num_tokens, mf_stream_t stream);
+
 /* Programmatic dependent launch (process-wide, on by default).  When on, every
  * kernel is launched with the programmatic stream serialisation attribute: it
  * may be scheduled before the previous kernel in the stream has fully

@@ -25,7 +25,7 @@ __all__ = [
     "moe_finalize_rmsnorm", "tp_moe_finalize_rmsnorm", "beam_moe_finalize",
     "beam_moe_finalize_norm_residual_norm", "MoeFinalizeError",
     "device_status", "selftest_wait_timeout", "select_finalize_variant", "select_beam_variant",
-    "finalize_kernel_name", "beam_kernel_name",
+    "finalize_kernel_name", "beam_kernel_name", "finalize_data_movement",
     "version", "set_programmatic_launch", "programmatic_launch", "HIDDEN", "TOP_K",
 ]
 
@@ -81,6 +81,24 @@ def moe_finalize_rmsnorm(gemm2_permuted: torch.Tensor, expert_weights: torch.Ten
     """
     g, w, idx, nw, out = gemm2_permuted, expert_weights, expanded_idx_to_permuted_idx, \
         norm_weight, output
+    wdt, row_stride, dev = _finalize_operands(g, w, idx, out)
+    if nw.dim() != 1 or nw.dtype != _BF16 or not nw.is_contiguous():
+        raise ValueError("norm_weight must be a contiguous 1-D BF16 tensor")
+    if nw.shape[0] != out.shape[1]:
+        raise ValueError("norm_weight and output disagree on hidden")
+    if nw.device != dev:
+        raise ValueError("all tensors must be on the same CUDA device")
+    st = _on_device(dev, lib().moe_finalize_rmsnorm_variant,
+                    g.data_ptr(), g.shape[0], row_stride, w.data_ptr(), wdt, idx.data_ptr(),
+                    nw.data_ptr(), out.data_ptr(), out.shape[0], out.shape[1], idx.shape[1],
+                    float(eps), float(gain_center), 1 if weight_before_norm else 0,
+                    _variant(variant), _stream_ptr(stream, dev))
+    check(st, "moe_finalize_rmsnorm")
+
+
+def _finalize_operands(g, w, idx, out):
+    """Metadata checks shared by the finalize calls; returns the weights' dtype
+    code, gemm2's row stride and the device."""
     gs, os_, ids = g.shape, out.shape, idx.shape
     wdt = _WEIGHT_DTYPES.get(w.dtype)
     if len(gs) != 2 or g.dtype != _BF16 or (g.stride(1) != 1 and gs[1] > 1):
@@ -92,26 +110,33 @@ def moe_finalize_rmsnorm(gemm2_permuted: torch.Tensor, expert_weights: torch.Ten
     if wdt is None or not w.is_contiguous() or w.shape != ids:
         raise ValueError("expert_weights must be contiguous BF16, FP32 or packed int32 with the "
                          "index map's shape")
-    if nw.dim() != 1 or nw.dtype != _BF16 or not nw.is_contiguous():
-        raise ValueError("norm_weight must be a contiguous 1-D BF16 tensor")
     if os_[0] != ids[0]:
         raise ValueError("output and the index map disagree on num_tokens")
-    if nw.shape[0] != os_[1]:
-        raise ValueError("norm_weight and output disagree on hidden")
     if gs[1] < os_[1]:
         # a narrowed view would otherwise let the kernel read past its columns
         raise ValueError("gemm2_permuted has fewer columns than output's hidden")
     dev = out.device
-    if dev.type != "cuda" or g.device != dev or w.device != dev or idx.device != dev or \
-            nw.device != dev:
+    if dev.type != "cuda" or g.device != dev or w.device != dev or idx.device != dev:
         raise ValueError("all tensors must be on the same CUDA device")
     row_stride = g.stride(0) if gs[0] > 1 else max(gs[1], g.stride(0))
-    st = _on_device(dev, lib().moe_finalize_rmsnorm_variant,
-                    g.data_ptr(), gs[0], row_stride, w.data_ptr(), wdt, idx.data_ptr(),
-                    nw.data_ptr(), out.data_ptr(), os_[0], os_[1], ids[1], float(eps),
-                    float(gain_center), 1 if weight_before_norm else 0, _variant(variant),
+    return wdt, row_stride, dev
+
+
+def finalize_data_movement(gemm2_permuted: torch.Tensor, expert_weights: torch.Tensor,
+                           expanded_idx_to_permuted_idx: torch.Tensor, output: torch.Tensor, *,
+                           stream: torch.cuda.Stream | None = None) -> None:
+    """Measurement aid: the memory traffic of ``moe_finalize_rmsnorm`` at hidden
+    4096 / top_k 8 on the same operands, without its arithmetic (``output``
+    receives a meaningless bit pattern).  Timed beside the finalize, it shows
+    what the finalize adds to the cost of the bytes themselves."""
+    g, w, idx, out = gemm2_permuted, expert_weights, expanded_idx_to_permuted_idx, output
+    if out.dim() != 2 or idx.dim() != 2 or out.shape[1] != HIDDEN or idx.shape[1] != TOP_K:
+        raise ValueError(f"the data-movement kernel covers hidden {HIDDEN} with top_k {TOP_K}")
+    wdt, row_stride, dev = _finalize_operands(g, w, idx, out)
+    st = _on_device(dev, lib().mf_finalize_data_movement, g.data_ptr(), g.shape[0], row_stride,
+                    w.data_ptr(), wdt, idx.data_ptr(), out.data_ptr(), out.shape[0],
                     _stream_ptr(stream, dev))
-    check(st, "moe_finalize_rmsnorm")
+    check(st, "finalize_data_movement")
 
 
 tp_moe_finalize_rmsnorm = moe_finalize_rmsnorm

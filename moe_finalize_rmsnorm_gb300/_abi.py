@@ -32,6 +32,7 @@ SIGNATURES = {
     "beam_moe_finalize_norm_residual_norm": (
         _int, [_vp, _i64, _vp, _i64, _vp, _i64, _i32, _i32, _f32, _vp, _f32, _int, _vp, _f32,
                _int, _f32, _f32, _vp, _vp, _vp]),
+    "mf_finalize_data_movement": (_int, [_vp, _i64, _i64, _vp, _int, _vp, _vp, _i64, _vp]),
     "mf_select_finalize_variant": (_int, [_i64, _i32, _i32]),
     "mf_select_beam_variant": (_int, [_i64, _i32, _i32]),
     "mf_finalize_kernel_name": (ctypes.c_char_p, [_i64, _i32, _i32, _int]),

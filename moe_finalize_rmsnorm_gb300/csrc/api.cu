@@ -202,6 +202,46 @@ mf_status moe_finalize_rmsnorm(const void *gemm2_permuted, int64_t rows, int64_t
                                         weight_before_norm, MF_VARIANT_AUTO, stream);
 }
 
+mf_status mf_finalize_data_movement(const void *gemm2_permuted, int64_t rows, int64_t row_stride,
+                                    const void *expert_weights, mf_dtype weights_dtype,
+                                    const int32_t *expanded_idx_to_permuted_idx, void *output,
+                                    int64_t num_tokens, mf_stream_t stream) {
+    if (num_tokens < 0 || rows < 0) return MF_ERR_SHAPE;
+    if (row_stride < mf::kTpHidden || row_stride % 8 != 0) return MF_ERR_SHAPE;
+    if (weights_dtype != MF_DTYPE_BF16 && weights_dtype != MF_DTYPE_FP32 &&
+        weights_dtype != MF_DTYPE_PACKED_TOPK)
+        return MF_ERR_DTYPE;
+    if (num_tokens == 0) return MF_OK;
+    if (!expert_weights || !expanded_idx_to_permuted_idx || !output || (rows > 0 && !gemm2_permuted))
+        return MF_ERR_NULL;
+    if (!aligned(gemm2_permuted, 16) || !aligned(expert_weights, 16) ||
+        !aligned(expanded_idx_to_permuted_idx, 16) || !aligned(output, 16))
+        return MF_ERR_ALIGN;
+    if (num_tokens > 0x7fffffffLL) return MF_ERR_SHAPE;  // one CTA per token
+
+    const DeviceInfo *d = nullptr;
+    mf_status st = device_info(&d);
+    if (st != MF_OK) return st;
+    mf::TpArgs a = {};
+    a.gemm2 = static_cast<const uint16_t *>(gemm2_permuted);
+    a.rows = rows;
+    a.ld = row_stride;
+    a.weights = expert_weights;
+    a.idx = expanded_idx_to_permuted_idx;
+    a.out = static_cast<uint16_t *>(output);
+    a.num_tokens = num_tokens;
+    a.hidden = mf::kTpHidden;
+    a.top_k = mf::kTpTopK;
+    a.status = d->status;
+    a.timeout_ns = kWaitLimitNs;
+    a.programmatic = g_programmatic.load() != 0;
+    const int wk = weights_dtype == MF_DTYPE_BF16   ? mf::kWeightBF16
+                   : weights_dtype == MF_DTYPE_FP32 ? mf::kWeightFP32
+                                                    : mf::kWeightPacked;
+    return from_launch(
+        mf::launch_tp_data_movement(a, wk, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity,
                                     const float *expert_weights, int64_t weight_rows,
                                     void *output, int64_t live_tokens, int32_t top_k,

@@ -79,6 +79,10 @@ cudaError_t launch_tp_bulk(const TpArgs &a, int weight_kind, int resident_ctas, 
 // Multi-token CTAs of the staged hidden-4096 kernel for a launch (0: one token
 // per CTA throughout).
 int64_t tp_bulk_groups(int64_t num_tokens, int64_t resident_ctas);
+// The hidden-4096 finalize's memory traffic without its arithmetic (a
+// measurement aid): one staged CTA per token, the output row is the XOR of the
+// words read.
+cudaError_t launch_tp_data_movement(const TpArgs &a, int weight_kind, cudaStream_t s);
 // Any hidden in 256..8192 (multiple of 256) and top-k in 1..32.
 cudaError_t launch_tp_generic(const TpArgs &a, int weight_kind, int smem_per_sm, int num_sms,
                               cudaStream_t s);

@@ -480,6 +480,81 @@ __global__ void __launch_bounds__(kBulkThreads, 3)
 }
 
 // ---------------------------------------------------------------------------
+// data movement alone (a measurement aid; not part of the operation)
+
+// The memory traffic of the hidden-4096 finalize without its arithmetic: one
+// CTA per token loads the route (index and weight of each slot), copies each
+// valid row into shared memory (one bulk copy and one mbarrier per row, as
+// tp_token_bulk_kernel), every thread reads its chunks of each row back, and
+// the token's output row goes out with the same streaming stores.  What it
+// stores is the XOR of the words read (the weights included), so the compiler
+// keeps every load and no floating-point work is done.  Timed on the same
+// buffers as the finalize, it shows what the reduction, the norm and the
+// scheduling of the finalize kernels cost on top of the bytes they move.
+template <int WK>
+__global__ void __launch_bounds__(kBulkThreads, 3) tp_data_movement_kernel(const TpArgs a) {
+    constexpr int NT = kBulkThreads, CPT = kBulkCPT;
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    __shared__ uint64_t bars[8];
+
+    const int64_t t = blockIdx.x;
+    const int tid = threadIdx.x;
+    const uint32_t rows_base = smem_u32(rows_smem);
+
+    pdl_wait();
+    int idx[8];
+    float w[8];
+    load_route<WK>(a, t, idx, w);
+    uint32_t mask = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mask |= (slot_valid(idx[k], a.rows) ? 1u : 0u) << k;
+    if (tid == 0) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mbar_init(smem_u32(&bars[k]), 1);
+        fence_mbar_init();
+        const uint64_t policy = policy_evict_first();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if ((mask >> k) & 1u) {
+                const uint32_t b = smem_u32(&bars[k]);
+                mbar_arrive_expect_tx(b, kTpRowBytes);
+                bulk_copy_g2s_hint(rows_base + k * kTpRowBytes,
+                                   a.gemm2 + static_cast<int64_t>(idx[k]) * a.ld, kTpRowBytes, b,
+                                   policy);
+            }
+    }
+    __syncthreads();  // the barriers are initialised before anyone waits on them
+
+    uint4 x[CPT];
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) x[c] = make_uint4(0u, 0u, 0u, 0u);
+    bool ok = true;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (!((mask >> k) & 1u)) continue;
+        const uint32_t b = smem_u32(&bars[k]);
+        if (!mbar_wait(b, 0u, a.timeout_ns)) {
+            atomicOr(a.status, kStatusWaitTimeout);
+            ok = false;
+            (void)mbar_wait(b, 0u, a.timeout_ns);  // bounded: the copy may land, or not, before exit
+        }
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+            const uint4 q = lds_16(rows_base + k * kTpRowBytes + (tid + c * NT) * kChunkBytes);
+            x[c].x ^= q.x ^ __float_as_uint(w[k]);
+            x[c].y ^= q.y;
+            x[c].z ^= q.z;
+            x[c].w ^= q.w;
+        }
+    }
+    if (ok) {
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+            st_cs_16(a.out + t * kTpHidden + static_cast<int64_t>(tid + c * NT) * kChunkElems, x[c]);
+    }
+}
+
+// ---------------------------------------------------------------------------
 // any hidden / top-k: one CTA per token, valid rows staged in pieces
 
 // Warp 0 reads the route (lane k holds slot k) and compacts the valid slots in
@@ -1055,6 +1130,9 @@ cudaError_t prepare_tp_kernels(int smem_optin, int smem_per_sm) {
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_multi_kernel<kWeightBF16>, kBulkSmem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_multi_kernel<kWeightFP32>, kBulkSmem);
     if (e == cudaSuccess) e = set_dyn_smem(tp_token_bulk_multi_kernel<kWeightPacked>, kBulkSmem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_data_movement_kernel<kWeightBF16>, kBulkSmem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_data_movement_kernel<kWeightFP32>, kBulkSmem);
+    if (e == cudaSuccess) e = set_dyn_smem(tp_data_movement_kernel<kWeightPacked>, kBulkSmem);
     constexpr int warp_smem1 = kWarpSliceBytes * warp_tokens_per_cta<1>();
     constexpr int warp_smem = kWarpSliceBytes * warp_tokens_per_cta<2>();  // CPW 2..4
     if (e == cudaSuccess) e = set_dyn_smem(tp_warp_bulk_kernel<1, kWeightBF16>, warp_smem1);
@@ -1163,6 +1241,16 @@ cudaError_t launch_tp_bulk(const TpArgs &a, int wk, int resident_ctas, cudaStrea
         case kWeightBF16: return launch_ex(tp_token_bulk_multi_kernel<kWeightBF16>, grid, block, kBulkSmem, s, 1, p, a, groups);
         case kWeightPacked: return launch_ex(tp_token_bulk_multi_kernel<kWeightPacked>, grid, block, kBulkSmem, s, 1, p, a, groups);
         default: return launch_ex(tp_token_bulk_multi_kernel<kWeightFP32>, grid, block, kBulkSmem, s, 1, p, a, groups);
+    }
+}
+
+cudaError_t launch_tp_data_movement(const TpArgs &a, int wk, cudaStream_t s) {
+    const bool p = a.programmatic;
+    const dim3 grid(static_cast<unsigned>(a.num_tokens)), block(kBulkThreads);
+    switch (wk) {
+        case kWeightBF16: return launch_ex(tp_data_movement_kernel<kWeightBF16>, grid, block, kBulkSmem, s, 1, p, a);
+        case kWeightPacked: return launch_ex(tp_data_movement_kernel<kWeightPacked>, grid, block, kBulkSmem, s, 1, p, a);
+        default: return launch_ex(tp_data_movement_kernel<kWeightFP32>, grid, block, kBulkSmem, s, 1, p, a);
     }
 }
 

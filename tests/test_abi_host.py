@@ -260,3 +260,29 @@ def test_kernel_names_without_a_device(lib):
     assert beam(10, 8, 7168, 1, 0) == "beam_token_cta_kernel"
     assert beam(10, 8, 512, 0, 0) == "beam_warp_bulk_kernel"
     assert beam(0, 8, 512, 0, 0) == beam(10, 33, 512, 0, 0) == ""
+
+
+def test_data_movement_validation(lib):
+    # the measurement aid takes the finalize's operands at hidden 4096 / top_k 8
+    def dm(gemm2=A, rows=100, stride=4096, w=A, wdt=1, idx=A, out=A, T=5):
+        return lib.mf_finalize_data_movement(gemm2, rows, stride, w, wdt, idx, out, T, None)
+    assert dm(stride=4095) == SHAPE
+    assert dm(stride=4100) == SHAPE
+    assert dm(T=-1) == SHAPE
+    assert dm(rows=-1) == SHAPE
+    assert dm(T=1 << 31) == SHAPE
+    assert dm(wdt=3) == DTYPE
+    for kw in ("gemm2", "w", "idx", "out"):
+        assert dm(**{kw: None}) == NULL, kw
+        assert dm(**{kw: MIS}) == ALIGN, kw
+    assert dm(gemm2=None, w=None, idx=None, out=None, T=0) == OK
+
+
+def test_binding_data_movement_covers_4096_by_8_only(monkeypatch):
+    import torch
+    import moe_finalize_rmsnorm_gb300 as mf
+    monkeypatch.setattr(mf, "lib", _no_library_call)
+    g = torch.zeros((16, 2048), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="hidden 4096"):
+        mf.finalize_data_movement(g, torch.ones((2, 8)), torch.zeros((2, 8), dtype=torch.int32),
+                                  torch.empty((2, 2048), dtype=torch.bfloat16))
