@@ -285,7 +285,7 @@ mf_status beam_moe_finalize_variant(const void *expert_outputs, int64_t capacity
 
     if (variant == MF_VARIANT_AUTO) variant = pick_beam(live_tokens);
     if (variant == MF_VARIANT_BULK)
-        return from_launch(mf::launch_beam_bulk(a, d->smem_per_sm, false, s));
+        return from_launch(mf::launch_beam_bulk(a, d->smem_per_sm, d->num_sms, false, s));
     return from_launch(mf::launch_beam_token_cta(a, s));
 }
 
@@ -347,7 +347,7 @@ mf_status beam_moe_finalize_norm_residual_norm(
     a.has_next = has_next_norm ? 1 : 0;
     a.scale_x = scale_x;
     a.scale_residual = scale_residual;
-    return from_launch(mf::launch_beam_bulk(a, d->smem_per_sm, true,
+    return from_launch(mf::launch_beam_bulk(a, d->smem_per_sm, d->num_sms, true,
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -403,7 +403,13 @@ const char *mf_beam_kernel_name(int64_t live_tokens, int32_t top_k, int32_t hidd
     if (variant == MF_VARIANT_AUTO || residual) variant = MF_VARIANT_BULK;
     if (variant == MF_VARIANT_TOKEN_CTA) return "beam_token_cta_kernel";
     if (variant != MF_VARIANT_BULK) return "";
-    return hidden <= 1024 ? "beam_warp_bulk_kernel" : "beam_token_bulk_kernel";
+    if (hidden <= 1024) return "beam_warp_bulk_kernel";
+    const DeviceInfo *d = nullptr;
+    if (device_info(&d) != MF_OK) d = nullptr;
+    return d != nullptr && mf::beam_bulk_groups(live_tokens, top_k, hidden, residual != 0,
+                                                d->smem_per_sm, d->num_sms) > 0
+               ? "beam_token_bulk_multi_kernel"
+               : "beam_token_bulk_kernel";
 }
 
 mf_variant mf_select_beam_variant(int64_t live_tokens, int32_t top_k, int32_t hidden) {

@@ -21,6 +21,10 @@
 //                          row, issued by lanes of warp 0 right after the
 //                          dependency wait (two CTAs per SM), then every thread
 //                          reduces its chunks from shared memory.
+//   beam_token_bulk_multi_kernel  the residual op at hidden 4096..7168 from five
+//                          waves of tokens: the staged kernel with three tokens
+//                          in each of the first CTAs, the next token's rows in
+//                          flight during the current token's epilogue.
 //   beam_warp_bulk_kernel  hidden 256..1024: the same with one warp per token
 //                          (one copy per piece of rows), four tokens per CTA.
 //
@@ -360,6 +364,134 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
     }
 }
 
+// The residual op's staged kernel with several tokens in each of the first
+// `groups` CTAs, for hidden 4096..7168 with two chunks per thread and a token
+// whose rows fit the buffer in one piece with a barrier per row.  CTA
+// b < groups takes kBeamTokensPerCta consecutive live tokens, the CTAs after it
+// one token each (the last kBeamSingleWaves waves).  Once every thread has read
+// the current token's rows, the lane of each row copies the next token's row
+// into the same buffer slot, before the current token's epilogue: the serial
+// end of each token (the post-norm RMS, the residual step, the next RMS and two
+// rows of stores) overlaps the next token's copies.  Each token's residual
+// chunks and the next token's weights are requested while its rows are in
+// flight; post_weight and next_weight only at the start of the epilogue, so
+// that no registers hold them across the row loop.  Each token's arithmetic is
+// that of beam_token_bulk_kernel: the same bits.  (For plain Beam, whose end of
+// token is one reduction, the same scheme measured slower.)
+constexpr int kBeamTokensPerCta = 3;
+constexpr int kBeamSingleWaves = 2;
+constexpr int kBeamMultiCPT = 2;
+// At most 448 threads (hidden 7168) so that two CTAs keep 72 registers per
+// thread: 512 threads would leave 64, and the kernel spills below 70.
+constexpr int kBeamMultiMaxThreads = 448;
+
+__global__ void __launch_bounds__(kBeamMultiMaxThreads, 2)
+    beam_token_bulk_multi_kernel(const BeamArgs a, const int64_t groups) {
+    constexpr int CPT = kBeamMultiCPT;
+    extern __shared__ __align__(128) uint8_t rows_smem[];
+    __shared__ uint64_t bars[32];
+    __shared__ float red[2][32];
+    __shared__ float red2[2][32];
+    __shared__ float wsm[2][32];
+    const int NT = blockDim.x;
+    const int tid = threadIdx.x;
+    const int64_t b = blockIdx.x;
+    const bool grouped = b < groups;
+    int64_t t = grouped ? kBeamTokensPerCta * b : (kBeamTokensPerCta - 1) * groups + b;
+    const int ntok = grouped ? kBeamTokensPerCta : 1;
+    const int K = a.top_k, H = a.hidden;
+    const uint32_t row_bytes = static_cast<uint32_t>(H) * 2;
+    const uint32_t base = smem_u32(rows_smem);
+
+    // lane r (< K) of warp 0 owns row r: its mbarrier and its copy of every token
+    auto issue_row = [&](int64_t tok) {
+        const uint32_t bb = smem_u32(&bars[tid]);
+        mbar_arrive_expect_tx(bb, row_bytes);
+        bulk_copy_g2s_hint(base + tid * row_bytes, a.x + (tok * K + tid) * static_cast<int64_t>(H),
+                           row_bytes, bb, policy_evict_first());
+    };
+    if (tid < K) {
+        mbar_init(smem_u32(&bars[tid]), 1);
+        fence_mbar_init();
+    }
+    pdl_wait();
+    if (tid < K) {
+        issue_row(t);
+        wsm[0][tid] = __ldg(a.weights + t * K + tid);
+    }
+    __syncthreads();  // barriers initialised, first weights stored
+
+    const bool norm = a.has_norm != 0;
+    uint32_t phase = 0;
+    for (int j = 0; j < ntok; ++j, ++t, phase ^= 1u) {
+        uint4 resq[CPT];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+            resq[c] = ld_na_16(a.residual + t * H + static_cast<int64_t>(tid + c * NT) * kChunkElems);
+        const bool has_next = j + 1 < ntok;
+        const float wnext = (has_next && tid < K) ? __ldg(a.weights + (t + 1) * K + tid) : 0.f;
+        const float *ws = wsm[j & 1];
+        float acc[CPT][8];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[c][e] = 0.f;
+        bool ok = true;
+        for (int r = 0; r < K; ++r) {
+            const uint32_t bb = smem_u32(&bars[r]);
+            if (!mbar_wait(bb, phase, a.timeout_ns)) {
+                atomicOr(a.status, kStatusWaitTimeout);
+                ok = false;
+                (void)mbar_wait(bb, phase, a.timeout_ns);  // bounded: the copy may land, or not, before exit
+            }
+            const float w = ws[r];
+            const uint32_t row = base + static_cast<uint32_t>(r) * row_bytes;
+            uint4 q[CPT];
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) q[c] = lds_16(row + (tid + c * NT) * kChunkBytes);
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) {
+                float x[8];
+                unpack8(q[c], x);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[c][e] = __fmaf_rn(w, x[e], acc[c][e]);
+            }
+        }
+        bool more = false;
+        if (has_next) {
+            // every thread has read the buffer and none gave up waiting: the
+            // next token's rows go in flight before this token's epilogue
+            if (tid < K) wsm[(j + 1) & 1][tid] = wnext;
+            more = !__syncthreads_or(!ok);
+            if (more && tid < K) {
+                fence_proxy_async_smem();  // the reads above come before the copies
+                issue_row(t + 1);
+            }
+        }
+        uint4 pwq[CPT], nwq[CPT];
+        load_post_weight<CPT>(a, tid, NT, pwq);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c)
+            nwq[c] = a.next_weight
+                         ? __ldg(reinterpret_cast<const uint4 *>(a.next_weight) + tid + c * NT)
+                         : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        round_scale_round<CPT>(acc, a.routed_scale);
+        float rs = 1.f;
+        if (norm) {
+            float *rd = red[j & 1];  // alternate: a slow warp may still read the last one
+            const float ss = warp_sum(sum_squares<CPT>(acc));
+            if ((tid & 31) == 0) rd[tid >> 5] = ss;
+            __syncthreads();
+            float tot = 0.f;
+            const int nw = NT >> 5;
+            for (int i = 0; i < nw; ++i) tot += rd[i];
+            rs = inv_rms(tot, H, a.post_eps);
+        }
+        residual_epilogue<CPT>(acc, pwq, resq, nwq, a, norm, rs, t, tid, NT, red2[j & 1], ok);
+        if (!more) break;
+    }
+}
+
 // ---------------------------------------------------------------------------
 // small hidden (256..1024): one warp per live token, four tokens per CTA
 
@@ -520,6 +652,7 @@ cudaError_t prepare_beam_kernels(int smem_per_sm) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, true, true>, attr, budget);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, false, true>, attr, budget);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, true, true>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_multi_kernel, attr, budget);
     return e;
 }
 
@@ -546,7 +679,37 @@ static cudaError_t launch_beam_warp(const BeamArgs &a, bool residual, cudaStream
     return launch_ex(beam_warp_bulk_kernel<CPW, false>, grid, block, bytes, s, 1, a.programmatic, a, rows);
 }
 
-cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, bool residual, cudaStream_t s) {
+static int beam_multi_per_sm(int threads, size_t bytes) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, beam_token_bulk_multi_kernel,
+                                                      threads, bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+int64_t beam_bulk_groups(int64_t live, int top_k, int hidden, bool residual, int smem_per_sm,
+                         int num_sms) {
+    // below hidden 4096 (2048..3584) the same scheme measured 0.7-1.5 % slower
+    // or the same: more CTAs per SM already cover each one's end of token
+    if (!residual || hidden < 4096 || beam_bulk_cpt(hidden) != kBeamMultiCPT || num_sms <= 0)
+        return 0;
+    const int threads = hidden / 16;
+    const int rows = beam_bulk_rows(smem_per_sm, top_k, hidden);
+    if (top_k > rows || threads > kBeamMultiMaxThreads) return 0;
+    const int64_t resident =
+        int64_t{beam_multi_per_sm(threads, static_cast<size_t>(rows) * hidden * 2)} * num_sms;
+    const int64_t n = kBeamTokensPerCta, singles = int64_t{kBeamSingleWaves} * resident;
+    if (resident <= 0 || live < singles + n * resident) return 0;
+    int64_t groups = (live - singles) / n;
+    const int64_t r = groups % resident;  // drop a partial wave that would outlast the rest
+    if (r != 0 && n * (resident - r) > singles) groups -= r;
+    return groups;
+}
+
+cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, int num_sms, bool residual,
+                             cudaStream_t s) {
     switch (a.hidden) {  // hidden 256..1024: one warp per token
         case 256: return launch_beam_warp<1>(a, residual, s);
         case 512: return launch_beam_warp<2>(a, residual, s);
@@ -559,6 +722,11 @@ cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, bool residual, 
     const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;
     const dim3 grid(static_cast<unsigned>(a.live)), block(a.hidden / 8 / cpt);
     const bool p = a.programmatic;
+    const int64_t groups = beam_bulk_groups(a.live, a.top_k, a.hidden, residual, smem_per_sm, num_sms);
+    if (groups > 0) {
+        const dim3 mgrid(static_cast<unsigned>(a.live - (kBeamTokensPerCta - 1) * groups));
+        return launch_ex(beam_token_bulk_multi_kernel, mgrid, block, bytes, s, 1, p, a, groups);
+    }
     // CPT 2 implies hidden >= 2048 (rows of 4 KB and more): per-row barriers
     if (cpt == 2) {
         if (residual) return launch_ex(beam_token_bulk_kernel<2, true, true>, grid, block, bytes, s, 1, p, a, rows);

@@ -96,7 +96,12 @@ int64_t tp_generic_groups(int64_t num_tokens, int hidden, int top_k, int weight_
 cudaError_t launch_beam_token_cta(const BeamArgs &a, cudaStream_t s);
 // `residual`: finalize, then the residual-add and next norm of
 // beam_moe_finalize_norm_residual_norm.
-cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, bool residual, cudaStream_t s);
+cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, int num_sms, bool residual,
+                             cudaStream_t s);
+// Multi-token CTAs of a staged Beam launch (0: one token per CTA throughout;
+// only the residual op at hidden 4096..7168 takes several tokens per CTA).
+int64_t beam_bulk_groups(int64_t live, int top_k, int hidden, bool residual, int smem_per_sm,
+                         int num_sms);
 
 cudaError_t launch_wait_timeout_selftest(unsigned *status, uint64_t timeout_ns, cudaStream_t s);
 

@@ -136,6 +136,41 @@ def test_fuzz_residual_norm(cuda_lib, seed):
         assert np.array_equal(h, rh)   # no norm on the way to hidden: bit-exact
 
 
+@pytest.mark.parametrize("seed", _seeds(4))
+def test_fuzz_residual_norm_many_tokens(cuda_lib, seed):
+    # token counts where the residual op takes three tokens per CTA (hidden
+    # 4096..7168 with two chunks per thread, a token in one piece)
+    import oracle
+    import test_parity_gpu as tpg
+    rng = np.random.default_rng(7000 + seed)
+    H = int(rng.choice([4096, 4608, 5120, 5632, 6144, 6656, 7168]))
+    K = int(rng.integers(1, 9))
+    T = int(rng.integers(2300, 3500))
+    post = bool(rng.random() < 0.7)
+    nxt = [None, "weighted", "plain"][int(rng.integers(0, 3))]
+    scales = None if rng.random() < 0.5 else (float(rng.choice([0.5, 1.25, -0.75])),
+                                               float(rng.choice([2.0, 1.0, -0.5])))
+    case = si.beam_case(f"rfuzzm{seed}", T + int(rng.integers(0, 5)), K, H, T,
+                        routed_scale=float(rng.choice([1.0, 2.5])), seed=seed,
+                        poison_dead_rows=True)
+    assert cuda_lib.beam_kernel_name(T, K, H, residual=True) == "beam_token_bulk_multi_kernel"
+    res = si.normal_bf16((T, H), float(rng.choice([0.5, 2.0])), seed, 9)
+    h, n, _ = tpg.run_residual(cuda_lib, case, res, post=post, nxt=nxt, scales=scales,
+                               inplace=bool(rng.random() < 0.3))
+    nw = case.post_weight[::-1].copy() if nxt == "weighted" else None
+    rh, rn = oracle.beam_moe_finalize_norm_residual_norm(
+        case.expert_outputs, case.weights, res, routed_scale=case.routed_scale,
+        post_weight=case.post_weight if post else None, post_eps=1e-6 if post else None,
+        next_weight=nw, next_eps=1e-5 if nxt else None, scales=scales)
+    eh, en = tpg.residual_bounds(case, rh, rn, post=post, scales=scales, next_eps=1e-5,
+                                 next_weight=nw)
+    compare_bf16(h, rh, extra=eh)
+    if nxt:
+        compare_bf16(n, rn, extra=en)
+    if not post:
+        assert np.array_equal(h, rh)
+
+
 def test_calls_from_several_host_threads(cuda_lib):
     # four host threads, each with its own stream and inputs, calling at once
     cases = [small_case_for_thread(i) for i in range(4)]

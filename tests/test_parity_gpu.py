@@ -151,7 +151,18 @@ def test_kernel_name_reports_the_multi_token_kernel(cuda_lib):
     assert cuda_lib.finalize_kernel_name(first) == "tp_token_bulk_multi_kernel"
     assert cuda_lib.finalize_kernel_name(32768) == "tp_token_bulk_multi_kernel"
     assert cuda_lib.finalize_kernel_name(32768, variant="token_cta") == "tp_token_cta_kernel"
-    assert cuda_lib.beam_kernel_name(8000, 8, 7168, residual=True) == "beam_token_bulk_kernel"
+    # the residual op takes three tokens per CTA from five waves (two CTAs per
+    # SM at hidden 7168); plain Beam keeps one token per CTA
+    first = 5 * 2 * sms
+    assert cuda_lib.beam_kernel_name(first - 1, 8, 7168, residual=True) == "beam_token_bulk_kernel"
+    assert cuda_lib.beam_kernel_name(first, 8, 7168, residual=True) == \
+        "beam_token_bulk_multi_kernel"
+    assert cuda_lib.beam_kernel_name(8000, 8, 7168, residual=True) == \
+        "beam_token_bulk_multi_kernel"
+    assert cuda_lib.beam_kernel_name(8000, 8, 7168) == "beam_token_bulk_kernel"
+    assert cuda_lib.beam_kernel_name(8000, 16, 7168, residual=True) == "beam_token_bulk_kernel"
+    assert cuda_lib.beam_kernel_name(8000, 8, 8192, residual=True) == "beam_token_bulk_kernel"
+    assert cuda_lib.beam_kernel_name(8000, 8, 3072, residual=True) == "beam_token_bulk_kernel"
 
 
 def test_multi_token_ctas_half_the_slots_invalid(cuda_lib):
@@ -756,24 +767,41 @@ def test_residual_norm_shapes_and_in_place(cuda_lib, K, H):
     compare_bf16(n, rn, extra=en)
 
 
-@pytest.mark.parametrize("inplace", [False, True])
-def test_residual_norm_many_waves(cuda_lib, inplace):
-    # 1600 tokens at 7168 x 8 (five waves and more), in place and not
-    cap, K, H, T = 1603, 8, 7168, 1600
-    case = si.beam_case("resid_waves", cap, K, H, T, routed_scale=2.5, seed=64,
+MANY_WAVES = [  # T, H, K, post, next norm, scales, in place, expected kernel
+    (1600, 7168, 8, True, "weighted", (1.25, -0.75), False, "beam_token_bulk_multi_kernel"),
+    (1600, 7168, 8, True, "weighted", (1.25, -0.75), True, "beam_token_bulk_multi_kernel"),
+    (1700, 7168, 8, False, None, None, False, "beam_token_bulk_multi_kernel"),
+    (1650, 7168, 5, True, "plain", (0.5, 2.0), True, "beam_token_bulk_multi_kernel"),
+    (2500, 4096, 8, True, "weighted", None, False, "beam_token_bulk_multi_kernel"),
+    (2200, 5120, 6, True, "weighted", (1.25, -0.75), False, "beam_token_bulk_multi_kernel"),
+    (1000, 7168, 8, True, "weighted", (1.25, -0.75), False, "beam_token_bulk_kernel"),
+]
+
+
+@pytest.mark.parametrize("T,H,K,post,nxt,scales,inplace,kernel", MANY_WAVES)
+def test_residual_norm_many_waves(cuda_lib, T, H, K, post, nxt, scales, inplace, kernel):
+    # five waves of tokens and more: three tokens per CTA at hidden 4096..7168
+    # (with the post-norm off, the next norm off, the hidden output in place)
+    case = si.beam_case("resid_waves", T + 3, K, H, T, routed_scale=2.5, seed=64 + T + H,
                         poison_dead_rows=True)
-    assert cuda_lib.beam_kernel_name(T, K, H, residual=True) == "beam_token_bulk_kernel"
+    assert cuda_lib.beam_kernel_name(T, K, H, residual=True) == kernel
     res = si.normal_bf16((T, H), 1.0, 65, 1)
-    h, n, nw = run_residual(cuda_lib, case, res, post=True, nxt="weighted", scales=(1.25, -0.75),
-                            inplace=inplace)
+    nwt = case.post_weight[::-1].copy() if nxt == "weighted" else None
+    h, n, _ = run_residual(cuda_lib, case, res, post=post, nxt=nxt, scales=scales,
+                           inplace=inplace)
     rh, rn = oracle.beam_moe_finalize_norm_residual_norm(
-        case.expert_outputs, case.weights, res, routed_scale=2.5, post_weight=case.post_weight,
-        post_eps=1e-6, next_weight=case.post_weight[::-1].copy(), next_eps=1e-5,
-        scales=(1.25, -0.75))
-    eh, en = residual_bounds(case, rh, rn, post=True, scales=(1.25, -0.75), next_eps=1e-5,
-                             next_weight=case.post_weight[::-1].copy())
+        case.expert_outputs, case.weights, res, routed_scale=2.5,
+        post_weight=case.post_weight if post else None, post_eps=1e-6 if post else None,
+        next_weight=nwt, next_eps=1e-5 if nxt else None, scales=scales)
+    eh, en = residual_bounds(case, rh, rn, post=post, scales=scales, next_eps=1e-5,
+                             next_weight=nwt)
     compare_bf16(h, rh, extra=eh)
-    compare_bf16(n, rn, extra=en)
+    if nxt:
+        compare_bf16(n, rn, extra=en)
+    else:
+        assert n is None and rn is None
+    if not post:
+        assert np.array_equal(h, rh)
 
 
 def test_residual_norm_zero_tokens(cuda_lib):
