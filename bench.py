@@ -72,15 +72,23 @@ def reduce_max(value: float, group=None) -> float:
     return float(t.item())
 
 
+def code_only(text: str) -> str:
+    """C++ source without its comments, whitespace runs collapsed (the sources
+    hold no string literal with a comment marker)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def source_digest(kernel: str) -> str:
-    """Digest of the sources a kernel is built from (its family's .cu file and
-    the shared device headers); a recorded traffic figure applies only to the
-    sources it was measured on."""
+    """Digest of the code a kernel is built from (its family's .cu file and the
+    shared device headers, comments left out); a recorded traffic figure
+    applies only to the code it was measured on."""
     family = "beam_finalize.cu" if kernel.startswith("beam_") else "tp_finalize.cu"
     h = hashlib.sha256()
     for name in ("common.cuh", "kernels.h", family):
-        with open(os.path.join(CSRC, name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        with open(os.path.join(CSRC, name), encoding="utf-8") as f:
+            h.update(name.encode() + b"\0" + code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

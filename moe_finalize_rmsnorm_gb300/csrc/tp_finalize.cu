@@ -36,6 +36,14 @@
 //                        token and two tokens per CTA (small tokens would
 //                        otherwise make the grid CTA-launch bound); each
 //                        valid slot's lane copies its own row.
+//   *_multi_kernel       the three staged kernels above with three tokens in
+//                        each of the first CTAs (warps) of a launch of five
+//                        waves and more: the next token's route is loaded
+//                        while the current rows land, and its rows go in
+//                        flight before the current token's norm and stores.
+//   tp_data_movement_kernel  not part of the operation: the hidden-4096
+//                        finalize's memory traffic with no arithmetic, a
+//                        measuring stick for the kernels above.
 //
 // Routing weights may be BF16, FP32 or the producer's packed int32 routing
 // words (expert_id << 16) | bf16 weight bits (trtllm_fp8_per_tensor_scale_

@@ -190,3 +190,11 @@ def test_same_layout_copy_keeps_a_padded_row_stride():
     t = torch.arange(6 * 4160, dtype=torch.float32).view(6, 4160)[:, :4096]
     c = bench._same_layout_copy(torch, t)
     assert c.stride() == (4160, 1) and torch.equal(c, t) and c.data_ptr() != t.data_ptr()
+
+
+def test_source_digest_ignores_comments_only():
+    # a recorded traffic figure stays valid across comment edits, not code edits
+    a = "int x = 1; // one\n/* a block\n   comment */ int y;\n"
+    b = "int x = 1;\nint y;  // another comment\n"
+    assert bench.code_only(a) == bench.code_only(b) == "int x = 1; int y;"
+    assert bench.code_only("int x = 1;") != bench.code_only("int x = 2;")
