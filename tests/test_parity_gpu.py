@@ -691,6 +691,10 @@ def residual_bounds(case, h_ref, n_ref, *, post, scales, next_eps, next_weight):
     (about 1e-5 of elements); hidden = BF16(s0 f + s1 r) then differs by up to
     |s0| ulp(f) on top of its own rounding, which can be many ulps of hidden
     where s0 f and s1 r cancel.  The next norm scales that by rn * next_weight.
+    Each output's own BF16 round then adds up to half an ulp of the GPU's value
+    (at most 2^-8 of it) to that difference, which the plain bound, relative to
+    the oracle's value, does not cover where the oracle's value is 0 (s0 f and
+    s1 r cancelling exactly): the widening carries a factor 1 + 2^-7 for it.
     Without the post-norm f is bit-exact and no widening applies."""
     if not post:
         return None, None
@@ -699,13 +703,14 @@ def residual_bounds(case, h_ref, n_ref, *, post, scales, next_eps, next_weight):
                                      routed_scale=case.routed_scale,
                                      post_weight=case.post_weight, post_eps=1e-6)
     s0 = 1.0 if scales is None else scales[0]
+    own_round = 1.0 + 2.0 ** -7
     eh = abs(s0) * bf16_ulp(f_ref)
     if n_ref is None:
-        return eh, None
+        return eh * own_round, None
     hv = bf16_bits_to_f64(h_ref)
     rn = 1.0 / np.sqrt((hv * hv).mean(axis=1, keepdims=True) + next_eps)
     g = np.abs(bf16_bits_to_f64(next_weight)) if next_weight is not None else 1.0
-    return eh, (eh + bf16_ulp(h_ref)) * rn * g
+    return eh * own_round, (eh + bf16_ulp(h_ref)) * rn * g * own_round
 
 
 def run_residual(mf, case, residual_bits, *, post, nxt, scales, inplace=False, tokens=None):
