@@ -809,6 +809,67 @@ def test_residual_norm_many_waves(cuda_lib, T, H, K, post, nxt, scales, inplace,
         assert np.array_equal(h, rh)
 
 
+def test_residual_multi_token_ctas_after_a_producer_pdl_and_graph(cuda_lib):
+    # three tokens per CTA: the residual is written by a Beam call (no post-norm:
+    # bit-exact) right before each call on the same stream; programmatic launch
+    # off and on give the same bits, and so do two replays of a captured graph
+    T, K, H = 1700, 8, 7168
+    assert cuda_lib.beam_kernel_name(T, K, H, residual=True) == "beam_token_bulk_multi_kernel"
+    case = si.beam_case("resid_modes", T + 2, K, H, T, routed_scale=2.5, seed=90,
+                        poison_dead_rows=True)
+    src = si.beam_case("resid_modes_src", T, 2, H, T, routed_scale=1.5, post_weight=False,
+                       post_eps=None, seed=91)
+    x, w = dev_bf16(case.expert_outputs.reshape(-1, H)), torch.from_numpy(case.weights).cuda()
+    pw, nwt = dev_bf16(case.post_weight), case.post_weight[::-1].copy()
+    nw = dev_bf16(nwt)
+    xs, ws = dev_bf16(src.expert_outputs), torch.from_numpy(src.weights).cuda()
+    r = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    hid = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    nrm = torch.empty_like(hid)
+
+    def call():
+        cuda_lib.beam_moe_finalize(xs, ws, r, src.routed_scale)
+        cuda_lib.beam_moe_finalize_norm_residual_norm(x, w, r, pw, 1e-6, nw, 1e-5, (1.25, -0.75),
+                                                      2.5, hidden=hid, normalized=nrm)
+
+    def fresh():
+        for t in (r, hid, nrm):
+            t.fill_(float("nan"))
+        torch.cuda.synchronize()
+
+    got = {}
+    try:
+        for pdl in (False, True):
+            cuda_lib.set_programmatic_launch(pdl)
+            fresh()
+            call()
+            torch.cuda.synchronize()
+            got[pdl] = (host_bits(hid), host_bits(nrm))
+    finally:
+        cuda_lib.set_programmatic_launch(True)
+    assert all(np.array_equal(a, b) for a, b in zip(got[False], got[True]))
+    graph = torch.cuda.CUDAGraph()
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st), torch.cuda.graph(graph, stream=st):
+        call()
+    for _ in range(2):
+        fresh()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(hid), got[True][0])
+        assert np.array_equal(host_bits(nrm), got[True][1])
+    res_ref = oracle_beam(src)
+    rh, rn = oracle.beam_moe_finalize_norm_residual_norm(
+        case.expert_outputs, case.weights, res_ref, routed_scale=2.5,
+        post_weight=case.post_weight, post_eps=1e-6, next_weight=nwt, next_eps=1e-5,
+        scales=(1.25, -0.75))
+    eh, en = residual_bounds(case, rh, rn, post=True, scales=(1.25, -0.75), next_eps=1e-5,
+                             next_weight=nwt)
+    compare_bf16(got[True][0], rh, extra=eh)
+    compare_bf16(got[True][1], rn, extra=en)
+
+
 def test_residual_norm_zero_tokens(cuda_lib):
     case = si.beam_case("resid0", 4, 2, 256, 4, seed=63)
     x = dev_bf16(case.expert_outputs.reshape(8, 256))
