@@ -269,8 +269,9 @@ const char *mf_finalize_kernel_name(int64_t num_tokens, int32_t hidden, int32_t 
 
 /* The same for beam_moe_finalize_variant, and with nonzero `residual` for
  * beam_moe_finalize_norm_residual_norm: "beam_token_bulk_kernel",
- * "beam_token_bulk_multi_kernel" (the residual op at hidden 4096..7168 with
- * several tokens per CTA, from five waves of tokens up), "beam_warp_bulk_kernel"
+ * "beam_token_bulk_multi_kernel" (hidden 4096..7168, several tokens per CTA:
+ * the residual op from five waves of tokens up, plain Beam at small top_k or
+ * where one token per CTA leaves little data in flight), "beam_warp_bulk_kernel"
  * (hidden 256..1024) or "beam_token_cta_kernel". */
 const char *mf_beam_kernel_name(int64_t live_tokens, int32_t top_k, int32_t hidden,
                                 mf_variant variant, int residual);

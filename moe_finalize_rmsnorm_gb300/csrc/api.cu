@@ -406,8 +406,8 @@ const char *mf_beam_kernel_name(int64_t live_tokens, int32_t top_k, int32_t hidd
     if (hidden <= 1024) return "beam_warp_bulk_kernel";
     const DeviceInfo *d = nullptr;
     if (device_info(&d) != MF_OK) d = nullptr;
-    return d != nullptr && mf::beam_bulk_groups(live_tokens, top_k, hidden, residual != 0,
-                                                d->smem_per_sm, d->num_sms) > 0
+    return d != nullptr && mf::beam_bulk_multi(live_tokens, top_k, hidden, residual != 0,
+                                               d->smem_per_sm, d->num_sms)
                ? "beam_token_bulk_multi_kernel"
                : "beam_token_bulk_kernel";
 }

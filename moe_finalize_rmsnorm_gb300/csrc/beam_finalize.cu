@@ -21,10 +21,13 @@
 //                          row, issued by lanes of warp 0 right after the
 //                          dependency wait (two CTAs per SM), then every thread
 //                          reduces its chunks from shared memory.
-//   beam_token_bulk_multi_kernel  the residual op at hidden 4096..7168 from five
-//                          waves of tokens: the staged kernel with three tokens
-//                          in each of the first CTAs, the next token's rows in
-//                          flight during the current token's epilogue.
+//   beam_token_bulk_multi_kernel  hidden 4096..7168: the staged kernel with
+//                          several tokens per CTA and a ring of one or two token
+//                          slots, the next tokens' rows in flight during the
+//                          current token's epilogue (the residual op from five
+//                          waves of tokens; plain Beam where two tokens fit a
+//                          CTA's buffer or one token per CTA leaves little in
+//                          flight).
 //   beam_warp_bulk_kernel  hidden 256..1024: the same with one warp per token
 //                          (one copy per piece of rows), four tokens per CTA.
 //
@@ -364,73 +367,96 @@ __global__ void __launch_bounds__(beam_max_threads<CPT>(), CPT == 2 ? 2 : 1)
     }
 }
 
-// The residual op's staged kernel with several tokens in each of the first
-// `groups` CTAs, for hidden 4096..7168 with two chunks per thread and a token
-// whose rows fit the buffer in one piece with a barrier per row.  CTA
-// b < groups takes kBeamTokensPerCta consecutive live tokens, the CTAs after it
-// one token each (the last kBeamSingleWaves waves).  Once every thread has read
-// the current token's rows, the lane of each row copies the next token's row
-// into the same buffer slot, before the current token's epilogue: the serial
-// end of each token (the post-norm RMS, the residual step, the next RMS and two
-// rows of stores) overlaps the next token's copies.  Each token's residual
-// chunks and the next token's weights are requested while its rows are in
-// flight; post_weight and next_weight only at the start of the epilogue, so
-// that no registers hold them across the row loop.  Each token's arithmetic is
-// that of beam_token_bulk_kernel: the same bits.  (For plain Beam, whose end of
-// token is one reduction, the same scheme measured slower.)
-constexpr int kBeamTokensPerCta = 3;
-constexpr int kBeamSingleWaves = 2;
+// The staged kernel with several tokens per CTA and a ring of token slots, for
+// two chunks per thread (hidden 2048..7168, up to 448 threads) and a token
+// whose rows fit one slot with a barrier per row.  CTA b < groups takes n
+// consecutive live tokens, the CTAs after it u each (the last one fewer).  A
+// CTA first puts up to `slots` tokens in flight, one row copy per lane of warp
+// 0; once every thread has read a token's rows, those lanes copy the token
+// `slots` ahead into the same slot, before the current token's epilogue, so the
+// serial end of each token (its RMS reductions, the residual step, the stores)
+// overlaps row traffic.  The weights of a slot's token are stored by the lanes
+// that copy its rows, before they arm the row barriers (whose release orders
+// them before every reader's acquire).  Each token's arithmetic is that of
+// beam_token_bulk_kernel: the same bits.
+constexpr int kBeamTokensPerCta = 3;  // n = 3 x slots: as the finalize's multi-token kernels
+constexpr int kBeamSingleWaves = 2;   // waves of u-token CTAs at the end
 constexpr int kBeamMultiCPT = 2;
 // At most 448 threads (hidden 7168) so that two CTAs keep 72 registers per
-// thread: 512 threads would leave 64, and the kernel spills below 70.
+// thread: 512 threads would leave 64, fewer than the residual form needs.
 constexpr int kBeamMultiMaxThreads = 448;
+constexpr int kBeamMultiBars = 32;  // slots x top_k row barriers
 
+struct BeamMultiLayout {
+    int64_t groups;  // CTAs b < groups take n tokens, the later ones u
+    int n;
+    int u;
+    int slots;       // tokens whose rows the buffer holds at once
+};
+
+template <bool RESID>
 __global__ void __launch_bounds__(kBeamMultiMaxThreads, 2)
-    beam_token_bulk_multi_kernel(const BeamArgs a, const int64_t groups) {
+    beam_token_bulk_multi_kernel(const BeamArgs a, const BeamMultiLayout lay) {
     constexpr int CPT = kBeamMultiCPT;
     extern __shared__ __align__(128) uint8_t rows_smem[];
-    __shared__ uint64_t bars[32];
+    __shared__ uint64_t bars[kBeamMultiBars];
     __shared__ float red[2][32];
     __shared__ float red2[2][32];
-    __shared__ float wsm[2][32];
+    __shared__ float wsm[kBeamMultiBars];  // slot s, row r at s * K + r
     const int NT = blockDim.x;
     const int tid = threadIdx.x;
     const int64_t b = blockIdx.x;
-    const bool grouped = b < groups;
-    int64_t t = grouped ? kBeamTokensPerCta * b : (kBeamTokensPerCta - 1) * groups + b;
-    const int ntok = grouped ? kBeamTokensPerCta : 1;
-    const int K = a.top_k, H = a.hidden;
+    int64_t t0;
+    int cnt;
+    if (b < lay.groups) {
+        t0 = lay.n * b;
+        cnt = lay.n;
+    } else {
+        t0 = int64_t{lay.n} * lay.groups + int64_t{lay.u} * (b - lay.groups);
+        const int64_t left = a.live - t0;
+        cnt = left < lay.u ? static_cast<int>(left) : lay.u;
+    }
+    const int K = a.top_k, H = a.hidden, S = lay.slots;
     const uint32_t row_bytes = static_cast<uint32_t>(H) * 2;
+    const uint32_t token_bytes = row_bytes * static_cast<uint32_t>(K);
     const uint32_t base = smem_u32(rows_smem);
 
-    // lane r (< K) of warp 0 owns row r: its mbarrier and its copy of every token
-    auto issue_row = [&](int64_t tok) {
-        const uint32_t bb = smem_u32(&bars[tid]);
+    // lane s * K + r of warp 0 copies row r of the token in slot s
+    auto issue = [&](int slot, int r, int64_t tok) {
+        const uint32_t bb = smem_u32(&bars[slot * K + r]);
         mbar_arrive_expect_tx(bb, row_bytes);
-        bulk_copy_g2s_hint(base + tid * row_bytes, a.x + (tok * K + tid) * static_cast<int64_t>(H),
-                           row_bytes, bb, policy_evict_first());
+        bulk_copy_g2s_hint(base + slot * token_bytes + r * row_bytes,
+                           a.x + (tok * K + r) * static_cast<int64_t>(H), row_bytes, bb,
+                           policy_evict_first());
     };
-    if (tid < K) {
+    const int first = cnt < S ? cnt : S;
+    if (tid < S * K) {
         mbar_init(smem_u32(&bars[tid]), 1);
         fence_mbar_init();
     }
     pdl_wait();
-    if (tid < K) {
-        issue_row(t);
-        wsm[0][tid] = __ldg(a.weights + t * K + tid);
+    if (tid < first * K) {
+        const int slot = tid / K, r = tid - slot * K;
+        issue(slot, r, t0 + slot);
+        wsm[tid] = __ldg(a.weights + (t0 + slot) * K + r);
     }
+    uint4 pwq_cta[CPT];  // plain Beam: post_weight held across the tokens
+    if (!RESID) load_post_weight<CPT>(a, tid, NT, pwq_cta);
     __syncthreads();  // barriers initialised, first weights stored
 
     const bool norm = a.has_norm != 0;
+    int slot = 0;
     uint32_t phase = 0;
-    for (int j = 0; j < ntok; ++j, ++t, phase ^= 1u) {
+    for (int j = 0; j < cnt; ++j) {
+        const int64_t t = t0 + j;
         uint4 resq[CPT];
+        if (RESID) {  // this token's residual chunks, while its rows land
 #pragma unroll
-        for (int c = 0; c < CPT; ++c)
-            resq[c] = ld_na_16(a.residual + t * H + static_cast<int64_t>(tid + c * NT) * kChunkElems);
-        const bool has_next = j + 1 < ntok;
-        const float wnext = (has_next && tid < K) ? __ldg(a.weights + (t + 1) * K + tid) : 0.f;
-        const float *ws = wsm[j & 1];
+            for (int c = 0; c < CPT; ++c)
+                resq[c] = ld_na_16(a.residual + t * H + static_cast<int64_t>(tid + c * NT) * kChunkElems);
+        }
+        const bool refill = j + S < cnt;
+        const float wnext = (refill && tid < K) ? __ldg(a.weights + (t + S) * K + tid) : 0.f;
         float acc[CPT][8];
 #pragma unroll
         for (int c = 0; c < CPT; ++c)
@@ -438,14 +464,14 @@ __global__ void __launch_bounds__(kBeamMultiMaxThreads, 2)
             for (int e = 0; e < 8; ++e) acc[c][e] = 0.f;
         bool ok = true;
         for (int r = 0; r < K; ++r) {
-            const uint32_t bb = smem_u32(&bars[r]);
+            const uint32_t bb = smem_u32(&bars[slot * K + r]);
             if (!mbar_wait(bb, phase, a.timeout_ns)) {
                 atomicOr(a.status, kStatusWaitTimeout);
                 ok = false;
                 (void)mbar_wait(bb, phase, a.timeout_ns);  // bounded: the copy may land, or not, before exit
             }
-            const float w = ws[r];
-            const uint32_t row = base + static_cast<uint32_t>(r) * row_bytes;
+            const float w = wsm[slot * K + r];
+            const uint32_t row = base + slot * token_bytes + static_cast<uint32_t>(r) * row_bytes;
             uint4 q[CPT];
 #pragma unroll
             for (int c = 0; c < CPT; ++c) q[c] = lds_16(row + (tid + c * NT) * kChunkBytes);
@@ -457,24 +483,32 @@ __global__ void __launch_bounds__(kBeamMultiMaxThreads, 2)
                 for (int e = 0; e < 8; ++e) acc[c][e] = __fmaf_rn(w, x[e], acc[c][e]);
             }
         }
-        bool more = false;
-        if (has_next) {
-            // every thread has read the buffer and none gave up waiting: the
-            // next token's rows go in flight before this token's epilogue
-            if (tid < K) wsm[(j + 1) & 1][tid] = wnext;
+        bool more = true;
+        if (refill) {
+            // every thread has read this slot and none gave up waiting: the
+            // token `slots` ahead goes in flight into it before this epilogue
             more = !__syncthreads_or(!ok);
             if (more && tid < K) {
-                fence_proxy_async_smem();  // the reads above come before the copies
-                issue_row(t + 1);
+                wsm[slot * K + tid] = wnext;
+                fence_proxy_async_smem();  // the reads above come before the copy
+                issue(slot, tid, t + S);
             }
         }
         uint4 pwq[CPT], nwq[CPT];
-        load_post_weight<CPT>(a, tid, NT, pwq);
+        if (RESID) {
+            // post_weight and next_weight (the same for every token, so mostly
+            // cache hits) are requested here, not across the row loop, to
+            // spare registers
+            load_post_weight<CPT>(a, tid, NT, pwq);
 #pragma unroll
-        for (int c = 0; c < CPT; ++c)
-            nwq[c] = a.next_weight
-                         ? __ldg(reinterpret_cast<const uint4 *>(a.next_weight) + tid + c * NT)
-                         : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+            for (int c = 0; c < CPT; ++c)
+                nwq[c] = a.next_weight
+                             ? __ldg(reinterpret_cast<const uint4 *>(a.next_weight) + tid + c * NT)
+                             : make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
+        } else {
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) pwq[c] = pwq_cta[c];
+        }
         round_scale_round<CPT>(acc, a.routed_scale);
         float rs = 1.f;
         if (norm) {
@@ -487,8 +521,16 @@ __global__ void __launch_bounds__(kBeamMultiMaxThreads, 2)
             for (int i = 0; i < nw; ++i) tot += rd[i];
             rs = inv_rms(tot, H, a.post_eps);
         }
-        residual_epilogue<CPT>(acc, pwq, resq, nwq, a, norm, rs, t, tid, NT, red2[j & 1], ok);
+        if (RESID) {
+            residual_epilogue<CPT>(acc, pwq, resq, nwq, a, norm, rs, t, tid, NT, red2[j & 1], ok);
+        } else if (ok) {
+            beam_store<CPT>(acc, pwq, norm, rs, a.out + t * H, tid, NT);
+        }
         if (!more) break;
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
+        }
     }
 }
 
@@ -652,7 +694,8 @@ cudaError_t prepare_beam_kernels(int smem_per_sm) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<1, true, true>, attr, budget);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, false, true>, attr, budget);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, true, true>, attr, budget);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_multi_kernel, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_multi_kernel<false>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_multi_kernel<true>, attr, budget);
     return e;
 }
 
@@ -679,9 +722,10 @@ static cudaError_t launch_beam_warp(const BeamArgs &a, bool residual, cudaStream
     return launch_ex(beam_warp_bulk_kernel<CPW, false>, grid, block, bytes, s, 1, a.programmatic, a, rows);
 }
 
+template <bool RESID>
 static int beam_multi_per_sm(int threads, size_t bytes) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, beam_token_bulk_multi_kernel,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, beam_token_bulk_multi_kernel<RESID>,
                                                       threads, bytes) != cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
@@ -689,23 +733,73 @@ static int beam_multi_per_sm(int threads, size_t bytes) {
     return n;
 }
 
-int64_t beam_bulk_groups(int64_t live, int top_k, int hidden, bool residual, int smem_per_sm,
-                         int num_sms) {
-    // below hidden 4096 (2048..3584) the same scheme measured 0.7-1.5 % slower
-    // or the same: more CTAs per SM already cover each one's end of token
-    if (!residual || hidden < 4096 || beam_bulk_cpt(hidden) != kBeamMultiCPT || num_sms <= 0)
+template <bool RESID>
+static int beam_one_per_sm(int threads, size_t bytes) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, beam_token_bulk_kernel<kBeamMultiCPT, RESID, true>, threads, bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
         return 0;
-    const int threads = hidden / 16;
-    const int rows = beam_bulk_rows(smem_per_sm, top_k, hidden);
-    if (top_k > rows || threads > kBeamMultiMaxThreads) return 0;
-    const int64_t resident =
-        int64_t{beam_multi_per_sm(threads, static_cast<size_t>(rows) * hidden * 2)} * num_sms;
-    const int64_t n = kBeamTokensPerCta, singles = int64_t{kBeamSingleWaves} * resident;
-    if (resident <= 0 || live < singles + n * resident) return 0;
-    int64_t groups = (live - singles) / n;
-    const int64_t r = groups % resident;  // drop a partial wave that would outlast the rest
-    if (r != 0 && n * (resident - r) > singles) groups -= r;
-    return groups;
+    }
+    return n;
+}
+
+// Layout of a launch of the several-tokens kernel (slots 0: one token per CTA
+// instead).  It runs at the one-token kernel's CTAs per SM, never fewer: where
+// its extra registers would cost a CTA per SM (hidden 4096 / 5120 at small
+// top_k) the concurrency of more CTAs measured faster.  The residual op holds
+// one token per slot ring (more measured slower: its long epilogue, not the
+// bytes in flight, sets the pace); plain Beam holds two when two fit (at hidden
+// 7168 and top_k 1..4: 10-18 % faster than one token per CTA; four or eight
+// slots were slower than two), or one where one token per CTA leaves less than
+// 192 KB in flight per SM (hidden 5120 / 5632 at top_k 8: 2-4 % faster; with
+// more in flight the same or slower).
+static BeamMultiLayout beam_multi_layout(int64_t live, int top_k, int hidden, bool residual,
+                                         int smem_per_sm, int num_sms) {
+    BeamMultiLayout lay = {0, 0, 0, 0};
+    const int threads = hidden / 8 / kBeamMultiCPT;
+    // hidden 2048..3584 (more CTAs per SM) measured the same or 0.7-1.5 % slower
+    if (hidden < 4096 || beam_bulk_cpt(hidden) != kBeamMultiCPT || threads > kBeamMultiMaxThreads ||
+        num_sms <= 0 || live <= 0 || beam_bulk_rows(smem_per_sm, top_k, hidden) < top_k)
+        return lay;
+    const int64_t token_bytes = int64_t{top_k} * hidden * 2;
+    const int occ_one =
+        residual ? beam_one_per_sm<true>(threads, static_cast<size_t>(token_bytes))
+                 : beam_one_per_sm<false>(threads, static_cast<size_t>(token_bytes));
+    const int occ_multi =
+        residual ? beam_multi_per_sm<true>(threads, 0) : beam_multi_per_sm<false>(threads, 0);
+    if (occ_one <= 0 || occ_multi < occ_one) return lay;
+    int slots = static_cast<int>((smem_per_sm / occ_one - 2048) / token_bytes);
+    const int cap = residual ? 1 : 2;
+    if (slots > cap) slots = cap;
+    if (slots > kBeamMultiBars / top_k) slots = kBeamMultiBars / top_k;
+    if (slots < 1) return lay;
+    if (!residual && slots < 2 && occ_one * token_bytes >= 192 * 1024) return lay;
+    const int per_sm = residual ? beam_multi_per_sm<true>(threads, static_cast<size_t>(slots * token_bytes))
+                                : beam_multi_per_sm<false>(threads, static_cast<size_t>(slots * token_bytes));
+    const int64_t resident = int64_t{per_sm} * num_sms;
+    if (resident <= 0) return lay;
+    int64_t u = live / (4 * resident);  // later CTAs small enough for about four waves
+    if (u > slots) u = slots;
+    if (u < 1) u = 1;
+    const int64_t n = int64_t{kBeamTokensPerCta} * slots, singles = kBeamSingleWaves * u * resident;
+    int64_t groups = 0;
+    if (live >= singles + n * resident) {
+        groups = (live - singles) / n;
+        const int64_t r = groups % resident;  // drop a partial wave that would outlast the rest
+        if (r != 0 && n * (resident - r) > singles) groups -= r;
+    }
+    if (groups == 0 && u == 1) return lay;  // one token per CTA throughout
+    lay.groups = groups;
+    lay.n = static_cast<int>(n);
+    lay.u = static_cast<int>(u);
+    lay.slots = slots;
+    return lay;
+}
+
+bool beam_bulk_multi(int64_t live, int top_k, int hidden, bool residual, int smem_per_sm,
+                     int num_sms) {
+    return beam_multi_layout(live, top_k, hidden, residual, smem_per_sm, num_sms).slots > 0;
 }
 
 cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, int num_sms, bool residual,
@@ -722,10 +816,13 @@ cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, int num_sms, bo
     const size_t bytes = static_cast<size_t>(rows) * a.hidden * 2;
     const dim3 grid(static_cast<unsigned>(a.live)), block(a.hidden / 8 / cpt);
     const bool p = a.programmatic;
-    const int64_t groups = beam_bulk_groups(a.live, a.top_k, a.hidden, residual, smem_per_sm, num_sms);
-    if (groups > 0) {
-        const dim3 mgrid(static_cast<unsigned>(a.live - (kBeamTokensPerCta - 1) * groups));
-        return launch_ex(beam_token_bulk_multi_kernel, mgrid, block, bytes, s, 1, p, a, groups);
+    const BeamMultiLayout lay = beam_multi_layout(a.live, a.top_k, a.hidden, residual, smem_per_sm, num_sms);
+    if (lay.slots > 0) {
+        const int64_t ctas = lay.groups + (a.live - int64_t{lay.n} * lay.groups + lay.u - 1) / lay.u;
+        const size_t mbytes = static_cast<size_t>(lay.slots) * a.top_k * a.hidden * 2;
+        if (residual)
+            return launch_ex(beam_token_bulk_multi_kernel<true>, dim3(static_cast<unsigned>(ctas)), block, mbytes, s, 1, p, a, lay);
+        return launch_ex(beam_token_bulk_multi_kernel<false>, dim3(static_cast<unsigned>(ctas)), block, mbytes, s, 1, p, a, lay);
     }
     // CPT 2 implies hidden >= 2048 (rows of 4 KB and more): per-row barriers
     if (cpt == 2) {

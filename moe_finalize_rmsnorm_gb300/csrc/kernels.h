@@ -98,10 +98,9 @@ cudaError_t launch_beam_token_cta(const BeamArgs &a, cudaStream_t s);
 // beam_moe_finalize_norm_residual_norm.
 cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, int num_sms, bool residual,
                              cudaStream_t s);
-// Multi-token CTAs of a staged Beam launch (0: one token per CTA throughout;
-// only the residual op at hidden 4096..7168 takes several tokens per CTA).
-int64_t beam_bulk_groups(int64_t live, int top_k, int hidden, bool residual, int smem_per_sm,
-                         int num_sms);
+// Whether a staged Beam launch runs the several-tokens-per-CTA kernel.
+bool beam_bulk_multi(int64_t live, int top_k, int hidden, bool residual, int smem_per_sm,
+                     int num_sms);
 
 cudaError_t launch_wait_timeout_selftest(unsigned *status, uint64_t timeout_ns, cudaStream_t s);
 

@@ -105,6 +105,28 @@ def test_fuzz_beam(cuda_lib, seed):
         compare_bf16(run_beam(cuda_lib, case, v), ref)
 
 
+@pytest.mark.parametrize("seed", _seeds(4))
+def test_fuzz_beam_many_tokens(cuda_lib, seed):
+    # token counts and sizes where plain Beam may take several tokens per CTA
+    # (hidden 5120..7168 with two chunks per thread, a token in one piece)
+    rng = np.random.default_rng(8000 + seed)
+    H = int(rng.choice([5120, 5632, 6144, 6656, 7168]))
+    K = int(rng.integers(1, 9))
+    T = int(rng.integers(2500, 4000))
+    norm = bool(rng.random() < 0.7)
+    weighted = bool(rng.random() < 0.8) and norm  # post_weight only with the norm
+    case = si.beam_case(f"bfuzzm{seed}", T + int(rng.integers(0, 5)), K, H, T,
+                        routed_scale=float(rng.choice([1.0, 2.5])), seed=seed,
+                        post_weight=weighted, post_eps=1e-6 if norm else None,
+                        poison_dead_rows=True)
+    assert cuda_lib.beam_kernel_name(T, K, H) in ("beam_token_bulk_kernel",
+                                                  "beam_token_bulk_multi_kernel")
+    got, ref = run_beam(cuda_lib, case, "auto"), oracle_beam(case)
+    compare_bf16(got, ref)
+    if not norm:
+        assert np.array_equal(got, ref)
+
+
 @pytest.mark.parametrize("seed", _seeds(16))
 def test_fuzz_residual_norm(cuda_lib, seed):
     import oracle

@@ -518,13 +518,34 @@ def test_beam_shapes(cuda_lib, K, H, variant):
 
 
 # Beam launches of many waves with the token in one staged piece, at hidden
-# 2048-7168 with two chunks per thread or one (2304), dead rows poisoned.
-@pytest.mark.parametrize("T,H,K", [(1600, 7168, 8), (6000, 2048, 8), (4000, 4096, 4),
-                                   (3000, 2304, 8)])
-def test_beam_many_waves(cuda_lib, T, H, K):
-    case = si.beam_case(f"bwaves{T}", T + 7, K, H, T, routed_scale=2.5, seed=T + H,
+# 2048-7168 with two chunks per thread or one (2304), dead rows poisoned; the
+# several-tokens kernel with two token slots (top_k 1..6 at hidden 7168: CTAs
+# of two tokens only, or three-slot-deep groups first) or one (5120 x 8).
+ONE, MULTI = "beam_token_bulk_kernel", "beam_token_bulk_multi_kernel"
+
+
+@pytest.mark.parametrize("T,H,K,kernel", [
+    (1600, 7168, 8, ONE), (6000, 2048, 8, ONE), (4000, 4096, 4, ONE), (3000, 2304, 8, ONE),
+    (2600, 7168, 1, MULTI), (3100, 7168, 1, MULTI), (2500, 7168, 4, MULTI),
+    (5000, 7168, 2, MULTI), (3000, 7168, 3, MULTI), (6000, 5120, 8, MULTI),
+    (3000, 5632, 8, MULTI), (4000, 6656, 6, MULTI), (1000, 7168, 2, ONE)])
+def test_beam_many_waves(cuda_lib, T, H, K, kernel):
+    case = si.beam_case(f"bwaves{T}", T + 7, K, H, T, routed_scale=2.5, seed=T + H + K,
                         poison_dead_rows=True)
-    assert cuda_lib.beam_kernel_name(T, K, H) == "beam_token_bulk_kernel"
+    assert cuda_lib.beam_kernel_name(T, K, H) == kernel
+    compare_bf16(run_beam(cuda_lib, case, "auto"), oracle_beam(case))
+
+
+def test_beam_multi_token_ctas_without_norm_and_unweighted(cuda_lib):
+    # the several-tokens kernel with the post-norm off (bit-exact) and an
+    # unweighted post-norm
+    T, H, K = 3100, 7168, 2
+    assert cuda_lib.beam_kernel_name(T, K, H) == MULTI
+    case = si.beam_case("bmulti_nonorm", T, K, H, T, routed_scale=1.5, post_weight=False,
+                        post_eps=None, seed=77)
+    assert np.array_equal(run_beam(cuda_lib, case, "auto"), oracle_beam(case))
+    case = si.beam_case("bmulti_unweighted", T, K, H, T, routed_scale=1.5, post_weight=False,
+                        post_eps=1e-6, seed=78)
     compare_bf16(run_beam(cuda_lib, case, "auto"), oracle_beam(case))
 
 
@@ -778,7 +799,9 @@ MANY_WAVES = [  # T, H, K, post, next norm, scales, in place, expected kernel
     (1700, 7168, 8, False, None, None, False, "beam_token_bulk_multi_kernel"),
     (1650, 7168, 5, True, "plain", (0.5, 2.0), True, "beam_token_bulk_multi_kernel"),
     (2500, 4096, 8, True, "weighted", None, False, "beam_token_bulk_multi_kernel"),
-    (2200, 5120, 6, True, "weighted", (1.25, -0.75), False, "beam_token_bulk_multi_kernel"),
+    (2200, 5632, 6, True, "weighted", (1.25, -0.75), False, "beam_token_bulk_multi_kernel"),
+    # its extra registers would cost a CTA per SM here: one token per CTA
+    (2200, 5120, 6, True, "weighted", (1.25, -0.75), False, "beam_token_bulk_kernel"),
     (1000, 7168, 8, True, "weighted", (1.25, -0.75), False, "beam_token_bulk_kernel"),
 ]
 
