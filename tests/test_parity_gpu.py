@@ -431,8 +431,12 @@ def test_generic_sizes(cuda_lib, H, K, wdt):
 # several tokens per CTA (tp_generic_bulk_multi_kernel): hidden 7168 x 8 from
 # 1520 tokens on GB300 (two CTAs per SM), 3072 x 8 and 2304 x 8 (one chunk per
 # thread), 1280 x 10 (small rows, ten per piece); 5% invalid slots.
+# With small tokens at hidden 2048..7168 (top_k 1..3) the buffer holds two
+# tokens: 8000 x 7168 x 1, 7000 x 7168 x 2, 6000 x 6144 x 3, 16000 x 4096 x 1,
+# 16000 x 2048 x 2.
 @pytest.mark.parametrize("T,H,K", [(1600, 7168, 8), (4000, 3072, 8), (5000, 2304, 8),
-                                   (9000, 1280, 10)])
+                                   (9000, 1280, 10), (8000, 7168, 1), (7000, 7168, 2),
+                                   (6000, 6144, 3), (16000, 4096, 1), (16000, 2048, 2)])
 @pytest.mark.parametrize("wdt", ["fp32", "bf16", "packed"])
 def test_generic_multi_token_ctas(cuda_lib, T, H, K, wdt):
     case = si.tp_case(f"gmulti{T}{wdt}", T, hidden=H, top_k=K, indexed_rows=T * K + 5,
@@ -471,6 +475,21 @@ def test_generic_multi_token_ctas_half_the_slots_invalid(cuda_lib):
     case = si.tp_case("gmulti_sparse", T, hidden=H, top_k=K, indexed_rows=T * K,
                       invalid_frac=0.5, weights_dtype="fp32", seed=9)
     compare_bf16(run_tp(cuda_lib, case, "bulk"), oracle_tp(case))
+
+
+def test_generic_two_token_slots_with_empty_tokens(cuda_lib):
+    # two token slots at 7168 x 2 with half the slots invalid: about a quarter
+    # of the tokens have no valid row (their slot's barriers do not move on)
+    # and give exactly zero
+    T, H, K = 8000, 7168, 2
+    case = si.tp_case("gtwo_sparse", T, hidden=H, top_k=K, indexed_rows=T * K,
+                      invalid_frac=0.5, weights_dtype="bf16", weight_before_norm=True, seed=12)
+    empty = np.all((case.idx < 0) | (case.idx >= case.gemm2.shape[0]), axis=1)
+    assert empty.sum() > 1000
+    assert cuda_lib.finalize_kernel_name(T, H, K) == "tp_generic_bulk_multi_kernel"
+    got = run_tp(cuda_lib, case, "auto")
+    compare_bf16(got, oracle_tp(case))
+    assert np.all(got[empty] == 0)
 
 
 @pytest.mark.parametrize("variant", TP_VARIANTS)
