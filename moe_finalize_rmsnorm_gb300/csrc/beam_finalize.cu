@@ -392,10 +392,15 @@ struct BeamMultiLayout {
     int n;
     int u;
     int slots;       // tokens whose rows the buffer holds at once
+    int compact;     // plain Beam built for three CTAs per SM (fewer registers)
 };
 
-template <bool RESID>
-__global__ void __launch_bounds__(kBeamMultiMaxThreads, 2)
+// MINB 3 (plain Beam only): held to the registers of three 448-thread CTAs
+// (40, with a 16-byte spill), so that at hidden 4096..6656 it runs as many
+// CTAs per SM as the one-token kernel, which the 2-block build (59 registers)
+// does not.
+template <bool RESID, int MINB = 2>
+__global__ void __launch_bounds__(kBeamMultiMaxThreads, MINB)
     beam_token_bulk_multi_kernel(const BeamArgs a, const BeamMultiLayout lay) {
     constexpr int CPT = kBeamMultiCPT;
     extern __shared__ __align__(128) uint8_t rows_smem[];
@@ -695,6 +700,7 @@ cudaError_t prepare_beam_kernels(int smem_per_sm) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, false, true>, attr, budget);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_kernel<2, true, true>, attr, budget);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_multi_kernel<false>, attr, budget);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_multi_kernel<false, 3>, attr, budget);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(beam_token_bulk_multi_kernel<true>, attr, budget);
     return e;
 }
@@ -733,6 +739,16 @@ static int beam_multi_per_sm(int threads, size_t bytes) {
     return n;
 }
 
+static int beam_compact_per_sm(int threads, size_t bytes) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, beam_token_bulk_multi_kernel<false, 3>,
+                                                      threads, bytes) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
 template <bool RESID>
 static int beam_one_per_sm(int threads, size_t bytes) {
     int n = 0;
@@ -747,7 +763,12 @@ static int beam_one_per_sm(int threads, size_t bytes) {
 // Layout of a launch of the several-tokens kernel (slots 0: one token per CTA
 // instead).  It runs at the one-token kernel's CTAs per SM, never fewer: where
 // its extra registers would cost a CTA per SM (hidden 4096 / 5120 at small
-// top_k) the concurrency of more CTAs measured faster.  The residual op holds
+// top_k) the concurrency of more CTAs measured faster.  Plain Beam may then use
+// the build held to three CTAs' registers, with two token slots, where one
+// token per CTA leaves under 80 KB in flight per SM (4096 x 1, 4608 x 1 / 2,
+// 5632 x 1 / 2, 6144 x 2, 6656 x 2: 3-20 % faster); with more in flight its
+// spill and fewer registers cost more than the slots gain (4096 x 2: -2 %,
+// 6144 x 3: -7 %).  The residual op holds
 // one token per slot ring (more measured slower: its long epilogue, not the
 // bytes in flight, sets the pace); plain Beam holds two when two fit (at hidden
 // 7168 and top_k 1..4: 10-18 % faster than one token per CTA; four or eight
@@ -756,7 +777,7 @@ static int beam_one_per_sm(int threads, size_t bytes) {
 // more in flight the same or slower).
 static BeamMultiLayout beam_multi_layout(int64_t live, int top_k, int hidden, bool residual,
                                          int smem_per_sm, int num_sms) {
-    BeamMultiLayout lay = {0, 0, 0, 0};
+    BeamMultiLayout lay = {0, 0, 0, 0, 0};
     const int threads = hidden / 8 / kBeamMultiCPT;
     // hidden 2048..3584 (more CTAs per SM) measured the same or 0.7-1.5 % slower
     if (hidden < 4096 || beam_bulk_cpt(hidden) != kBeamMultiCPT || threads > kBeamMultiMaxThreads ||
@@ -768,15 +789,23 @@ static BeamMultiLayout beam_multi_layout(int64_t live, int top_k, int hidden, bo
                  : beam_one_per_sm<false>(threads, static_cast<size_t>(token_bytes));
     const int occ_multi =
         residual ? beam_multi_per_sm<true>(threads, 0) : beam_multi_per_sm<false>(threads, 0);
-    if (occ_one <= 0 || occ_multi < occ_one) return lay;
+    int compact = 0;
+    if (occ_one <= 0) return lay;
+    if (occ_multi < occ_one) {
+        if (residual || beam_compact_per_sm(threads, 0) < occ_one) return lay;
+        compact = 1;
+    }
     int slots = static_cast<int>((smem_per_sm / occ_one - 2048) / token_bytes);
     const int cap = residual ? 1 : 2;
     if (slots > cap) slots = cap;
     if (slots > kBeamMultiBars / top_k) slots = kBeamMultiBars / top_k;
     if (slots < 1) return lay;
-    if (!residual && slots < 2 && occ_one * token_bytes >= 192 * 1024) return lay;
-    const int per_sm = residual ? beam_multi_per_sm<true>(threads, static_cast<size_t>(slots * token_bytes))
-                                : beam_multi_per_sm<false>(threads, static_cast<size_t>(slots * token_bytes));
+    if (!residual && slots < 2 && (compact || occ_one * token_bytes >= 192 * 1024)) return lay;
+    if (compact && occ_one * token_bytes >= 80 * 1024) return lay;
+    const size_t sbytes = static_cast<size_t>(slots * token_bytes);
+    const int per_sm = residual ? beam_multi_per_sm<true>(threads, sbytes)
+                       : compact ? beam_compact_per_sm(threads, sbytes)
+                                 : beam_multi_per_sm<false>(threads, sbytes);
     const int64_t resident = int64_t{per_sm} * num_sms;
     if (resident <= 0) return lay;
     int64_t u = live / (4 * resident);  // later CTAs small enough for about four waves
@@ -794,6 +823,7 @@ static BeamMultiLayout beam_multi_layout(int64_t live, int top_k, int hidden, bo
     lay.n = static_cast<int>(n);
     lay.u = static_cast<int>(u);
     lay.slots = slots;
+    lay.compact = compact;
     return lay;
 }
 
@@ -822,6 +852,8 @@ cudaError_t launch_beam_bulk(const BeamArgs &a, int smem_per_sm, int num_sms, bo
         const size_t mbytes = static_cast<size_t>(lay.slots) * a.top_k * a.hidden * 2;
         if (residual)
             return launch_ex(beam_token_bulk_multi_kernel<true>, dim3(static_cast<unsigned>(ctas)), block, mbytes, s, 1, p, a, lay);
+        if (lay.compact)
+            return launch_ex(beam_token_bulk_multi_kernel<false, 3>, dim3(static_cast<unsigned>(ctas)), block, mbytes, s, 1, p, a, lay);
         return launch_ex(beam_token_bulk_multi_kernel<false>, dim3(static_cast<unsigned>(ctas)), block, mbytes, s, 1, p, a, lay);
     }
     // CPT 2 implies hidden >= 2048 (rows of 4 KB and more): per-row barriers

@@ -108,9 +108,9 @@ def test_fuzz_beam(cuda_lib, seed):
 @pytest.mark.parametrize("seed", _seeds(4))
 def test_fuzz_beam_many_tokens(cuda_lib, seed):
     # token counts and sizes where plain Beam may take several tokens per CTA
-    # (hidden 5120..7168 with two chunks per thread, a token in one piece)
+    # (hidden 4096..7168 with two chunks per thread, a token in one piece)
     rng = np.random.default_rng(8000 + seed)
-    H = int(rng.choice([5120, 5632, 6144, 6656, 7168]))
+    H = int(rng.choice([4096, 4608, 5120, 5632, 6144, 6656, 7168]))
     K = int(rng.integers(1, 9))
     T = int(rng.integers(2500, 4000))
     norm = bool(rng.random() < 0.7)

@@ -539,7 +539,8 @@ def test_beam_shapes(cuda_lib, K, H, variant):
 # Beam launches of many waves with the token in one staged piece, at hidden
 # 2048-7168 with two chunks per thread or one (2304), dead rows poisoned; the
 # several-tokens kernel with two token slots (top_k 1..6 at hidden 7168: CTAs
-# of two tokens only, or three-slot-deep groups first) or one (5120 x 8).
+# of two tokens only, or three-slot-deep groups first; small tokens at 4096..5632
+# in the build for three CTAs per SM) or one (5120 x 8).
 ONE, MULTI = "beam_token_bulk_kernel", "beam_token_bulk_multi_kernel"
 
 
@@ -547,7 +548,10 @@ ONE, MULTI = "beam_token_bulk_kernel", "beam_token_bulk_multi_kernel"
     (1600, 7168, 8, ONE), (6000, 2048, 8, ONE), (4000, 4096, 4, ONE), (3000, 2304, 8, ONE),
     (2600, 7168, 1, MULTI), (3100, 7168, 1, MULTI), (2500, 7168, 4, MULTI),
     (5000, 7168, 2, MULTI), (3000, 7168, 3, MULTI), (6000, 5120, 8, MULTI),
-    (3000, 5632, 8, MULTI), (4000, 6656, 6, MULTI), (1000, 7168, 2, ONE)])
+    (3000, 5632, 8, MULTI), (4000, 6656, 6, MULTI), (1000, 7168, 2, ONE),
+    # the build for three CTAs per SM (under 80 KB in flight with one token per CTA)
+    (16000, 4096, 1, MULTI), (8000, 4608, 1, MULTI), (8000, 5632, 2, MULTI),
+    (8000, 4096, 2, ONE), (6000, 6144, 3, ONE)])
 def test_beam_many_waves(cuda_lib, T, H, K, kernel):
     case = si.beam_case(f"bwaves{T}", T + 7, K, H, T, routed_scale=2.5, seed=T + H + K,
                         poison_dead_rows=True)
