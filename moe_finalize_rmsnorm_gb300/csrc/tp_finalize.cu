@@ -41,6 +41,10 @@
 //                        waves and more: the next token's route is loaded
 //                        while the current rows land, and its rows go in
 //                        flight before the current token's norm and stores.
+//                        The generic one holds two tokens at once (six per
+//                        CTA) when tokens are small (top_k 1..3 at large
+//                        hidden), where one token per CTA leaves little in
+//                        flight.
 //   tp_data_movement_kernel  not part of the operation: the hidden-4096
 //                        finalize's memory traffic with no arithmetic, a
 //                        measuring stick for the kernels above.
