@@ -492,6 +492,26 @@ def test_generic_two_token_slots_with_empty_tokens(cuda_lib):
     assert np.all(got[empty] == 0)
 
 
+def test_two_token_slot_kernels_with_and_without_programmatic_launch(cuda_lib):
+    # the generic finalize and Beam with two token slots per CTA give the same
+    # bits with programmatic launch off and on
+    tcase = si.tp_case("gtwo_pdl", 8000, hidden=7168, top_k=2, indexed_rows=16000,
+                       invalid_frac=0.05, weights_dtype="fp32", seed=14)
+    bcase = si.beam_case("btwo_pdl", 3100, 2, 7168, 3100, routed_scale=2.5, seed=15)
+    assert cuda_lib.finalize_kernel_name(8000, 7168, 2) == "tp_generic_bulk_multi_kernel"
+    assert cuda_lib.beam_kernel_name(3100, 2, 7168) == "beam_token_bulk_multi_kernel"
+    got = {}
+    try:
+        for pdl in (False, True):
+            cuda_lib.set_programmatic_launch(pdl)
+            got[pdl] = (run_tp(cuda_lib, tcase, "auto"), run_beam(cuda_lib, bcase, "auto"))
+    finally:
+        cuda_lib.set_programmatic_launch(True)
+    assert all(np.array_equal(a, b) for a, b in zip(got[False], got[True]))
+    compare_bf16(got[True][0], oracle_tp(tcase))
+    compare_bf16(got[True][1], oracle_beam(bcase))
+
+
 @pytest.mark.parametrize("variant", TP_VARIANTS)
 def test_packed_routing_words_specialised(cuda_lib, variant):
     case = si.tp_case("packed", 300, indexed_rows=2500, invalid_frac=0.03, weights_dtype="packed",
